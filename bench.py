@@ -1,0 +1,362 @@
+#!/usr/bin/env python
+"""MoE-layer decode throughput of the GB300 quantized routed-expert FFN.
+
+One step = one batch of T tokens through an L-layer stack of distinct MoE
+layers (each layer: quantise -> route -> routed + shared expert FFN), replayed
+from a CUDA graph.  Layers are timed as decode: each layer's kernels start
+after the previous layer's finish (stream order).  Every layer has its own
+seeded weights and hidden states, so a step touches L x (per-layer bytes) of
+HBM - far more than the 129 MB L2 - and no L2 flush is needed.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "MoE-layer decode tokens/s and achieved HBM GB/s vs ~8 TB/s peak (1xGB300)"
+UNIT = "layer-tok/s"
+DEFAULT_LAYERS = {"tiny": 64, "a3b": 40, "oss20b": 24, "wide": 8, "a22b": 48}
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="a3b")
+    p.add_argument("--layers", type=int, default=0)
+    p.add_argument("--tokens", type=int, default=1)
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "quantized_routed_expert_router_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel_key: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel sources are unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d.get(kernel_key)
+        if rec and rec.get("csrc_hash") == csrc_hash():
+            return float(rec["bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.p is not None:
+            time.sleep(0.2)
+            self.p.terminate()
+            try:
+                self.out, _ = self.p.communicate(timeout=5)
+            except Exception:
+                self.p.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), active=f[4], hw=f[5], hwt=f[6], swt=f[7],
+                                 pcap=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        smax = max(r["smax"] for r in rows)
+        load = [r for r in rows if r["sm"] >= 0.5 * smax] or rows
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def layer_bytes(cfg, dl, moe):
+    """Algorithmic HBM bytes of one layer-step: unique chosen experts + shared + router + activations."""
+    ids = dl.ids.cpu().numpy()
+    unique = len(np.unique(ids))
+    T = ids.shape[0]
+    per_expert = sum(dl.sizes)
+    shared = 0
+    if dl.shared is not None:
+        shared = (2 * moe.moe_packed_bytes(cfg.shared_qtype, cfg.shared_I, cfg.H)
+                  + moe.moe_packed_bytes(cfg.shared_qtype, cfg.H, cfg.shared_I))
+    bias = (2 * cfg.I + cfg.H) * 4 * unique if cfg.biases else 0
+    router = dl.router.numel() * dl.router.element_size()
+    act = T * cfg.H * 4 * 2 + T * cfg.k * 8
+    return dict(experts=unique * per_expert + bias, shared=shared, router=router, act=act, unique=unique,
+                total=unique * per_expert + bias + shared + router + act)
+
+
+def run_reference(args, cfg, L, rank, world):
+    import oracle
+    import synth
+    if rank != 0:
+        return
+    nsample = 2
+    layers = [synth.make_layer(cfg, l, T=args.tokens, seed=args.seed) for l in range(nsample)]
+    for i in range(args.warmup):
+        oracle.layer_forward(layers[i % nsample])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.layer_forward(layers[i % nsample])
+    dt = time.perf_counter() - t0
+    v = args.steps * args.tokens / dt
+    sample = (f"one {cfg.name} layer x {args.tokens} token(s) per step, cycling over {nsample} seeded layers; "
+              f"single-threaded scalar C oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32 dots + fp64 combine",
+            "data": "synthetic",
+            "config": {"workload": workload_name(cfg, L, args.tokens), "tokens": args.tokens, "layers": L},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_name(cfg, L, T):
+    return f"{cfg.name}: {cfg.note}; {L}-layer stack of distinct layers, {T} token(s) per step (decode)"
+
+
+def main():
+    args = parse()
+    import synth
+    cfg = synth.CONFIGS[args.config]
+    L = args.layers or DEFAULT_LAYERS.get(args.config, cfg.layers)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, cfg, L, rank, world)
+
+    import torch
+    import torch.distributed as dist
+    from quantized_routed_expert_router_gb300 import _build
+    _build.build()
+    import quantized_routed_expert_router_gb300 as moe
+    from quantized_routed_expert_router_gb300.device_layer import DeviceLayer
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    T = args.tokens
+
+    # ---- workload: L distinct layers, each rank its own tokens (seed offset)
+    t_gen = time.perf_counter()
+    layers, host_sample = [], []
+    for l in range(L):
+        Lh = synth.make_layer(cfg, l, T=T, seed=args.seed + 7919 * rank)
+        layers.append(DeviceLayer(Lh, dev))
+        if l < 2 and rank == 0 and not args.no_cpu:
+            host_sample.append(Lh)
+        del Lh
+    # one contiguous input and output buffer for the whole stack, so the
+    # end-to-end leg moves each step's inputs and results in one copy each
+    X = torch.empty((L, T, cfg.H), dtype=torch.float32, device=dev)
+    Y = torch.empty((L, T, cfg.H), dtype=torch.float32, device=dev)
+    for l, dl in enumerate(layers):
+        X[l].copy_(dl.x)
+        dl.x, dl.y = X[l], Y[l]
+    torch.cuda.synchronize()
+    gen_s = time.perf_counter() - t_gen
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(ffn_only=False, route_only=False):
+        for dl in layers:
+            if not ffn_only:
+                dl.quantize()
+                dl.route(logits=False)
+            if not route_only:
+                dl.ffn()
+
+    with torch.cuda.stream(stream):
+        step()                        # eager once: sets kernel attributes, fills ids
+    torch.cuda.synchronize()
+    bytes_l = [layer_bytes(cfg, dl, moe) for dl in layers]
+    step_bytes = sum(b["total"] for b in bytes_l)
+    ffn_bytes = sum(b["experts"] + b["shared"] for b in bytes_l)
+
+    graphs = {}
+    for name, kw in (("step", {}), ("ffn", {"ffn_only": True}), ("route", {"route_only": True})):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(**kw)
+        graphs[name] = g
+    torch.cuda.synchronize()
+
+    def timed(g, K, W):
+        for _ in range(W):
+            g.replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(K):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    K, W = args.steps, max(3, args.warmup)
+    with ClockSampler(local) as cs:
+        ms = timed(graphs["step"], K, W)
+    clocks = cs.summary()
+    ms_ffn = timed(graphs["ffn"], K, W)
+    ms_route = timed(graphs["route"], K, W)
+
+    # ---- end to end through the public API: pinned H2D of every layer's input,
+    # the captured public-API calls, D2H of every layer's y, per step
+    e2e = None
+    if not args.no_e2e:
+        xs = torch.empty((L, T, cfg.H), dtype=torch.float32).pin_memory()
+        ys = torch.empty((L, T, cfg.H), dtype=torch.float32).pin_memory()
+        xs.copy_(X.cpu())
+        ke = max(1, min(K, 500))
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for _ in range(ke):
+                X.copy_(xs, non_blocking=True)
+                graphs["step"].replay()
+                ys.copy_(Y, non_blocking=True)
+                stream.synchronize()
+        dt = time.perf_counter() - t0
+        if world > 1:
+            t = torch.tensor([dt], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": world * ke * L * T / dt, "unit": UNIT, "h2d_bytes_per_step": L * T * cfg.H * 4,
+               "d2h_bytes_per_step": L * T * cfg.H * 4, "steps": ke,
+               "mode": "pinned H2D + graph replay of the public C-ABI calls + D2H + stream sync, wall clock"}
+
+    value = world * K * L * T / (ms / 1e3)
+    peak, peak_src = peaks()
+    ffn_launch_ms = ms_ffn / (K * L)
+    achieved = (ffn_bytes / L) / (ffn_launch_ms / 1e3) / 1e9
+    traffic = traffic_record(f"moe_expert_ffn:{cfg.name}")
+    cpu = None
+    if rank == 0 and not args.no_cpu and host_sample:
+        import oracle
+        n = 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 10.0 and n < 40:
+            oracle.layer_forward(host_sample[n % len(host_sample)])
+            n += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": n * T / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n} layer-steps of {cfg.name} (T={T}) over {len(host_sample)} seeded layers, "
+                         f"single-threaded scalar C oracle, {dt:.1f} s"}
+    if rank == 0:
+        uniq = [b["unique"] for b in bytes_l]
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8 dp4a dots + fp32 combine (q4_K/q8_K)" if cfg.qtype == synth.Q4_K
+            else "int8 dp4a dots + fp32 combine",
+            "data": "synthetic",
+            "config": {"workload": workload_name(cfg, L, T), "tokens": T, "layers": L,
+                       "l2": f"inputs larger than L2: {step_bytes / 1e6:.0f} MB of distinct weights touched "
+                             f"per step (L2 129 MB)",
+                       "stack_tok_s": world * K * T / (ms / 1e3),
+                       "hbm_gbs": step_bytes * K / (ms / 1e3) / 1e9,
+                       "hbm_frac_of_measured": step_bytes * K / (ms / 1e3) / 1e9 / peak,
+                       "us_per_layer": 1e3 * ms / (K * L),
+                       "bytes_per_layer": step_bytes / L, "unique_experts_per_layer": float(np.mean(uniq)),
+                       "route_us_per_layer": 1e3 * ms_route / (K * L),
+                       "ffn_us_per_layer": 1e3 * ms_ffn / (K * L),
+                       "setup_s": gen_s},
+            "roofline": {"bound": "hbm", "kernel": "moe_expert_ffn (gateup_kernel + down_kernel)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_source": peak_src, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": ffn_bytes / L},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": K * L * 4,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

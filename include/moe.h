@@ -1,0 +1,245 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) quantized routed-expert MoE FFN.
+ *
+ * One decode step of a Mixture-of-Experts layer, as the pulsar README states
+ * it ("MoE resolve" passage and the model table):
+ *   1. moe_quantize_q8K : activations -> q8 blocks (integer dots follow,
+ *                         "activations quantized to q8_0/q8_K").
+ *   2. moe_route        : router GEMV, softmax or sigmoid top-k (README model
+ *                         table: "softmax router", "sigmoid-gated router").
+ *   3. moe_expert_ffn   : per (token, slot) the chosen expert's gate/up GEMVs
+ *                         over block-quantised weights, SwiGLU, requantised h,
+ *                         the down GEMV, the routing-weight scale and the
+ *                         fixed-order per-token sum, plus the shared expert.
+ *                         Experts arrive as explicit per-expert device
+ *                         pointers and a NULL gate pointer means "not mine"
+ *                         (README, "MoE resolve": the kernels receive
+ *                         per-(token, slot) pointers; NULL means not mine).
+ *
+ * Conventions for every call:
+ *  - All pointers named "device" are CUDA device pointers; the library never
+ *    dereferences them on the host.  Host pointers are marked "host".
+ *  - The caller owns every buffer.  The library allocates nothing, keeps no
+ *    state between calls and never synchronises the host, except
+ *    moe_read_device_status, which does.
+ *  - Calls are asynchronous and ordered on the given stream (0 = legacy
+ *    default stream).  Argument errors are returned before anything is
+ *    launched; a failed launch returns MOE_ERR_CUDA.
+ *  - Inputs must be finite.  Weights and expert tables are read-only for the
+ *    duration of a call.
+ *  - Results are deterministic: identical inputs give bit-identical outputs,
+ *    whatever the batch composition (see moe_expert_ffn).
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* NULL where a buffer is required, bad size or shape */
+    MOE_ERR_UNSUPPORTED = 2,   /* valid but not implemented (format/shape pairing)   */
+    MOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required          */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed                */
+    MOE_ERR_DEVICE_STATUS = 5, /* a kernel recorded a data error (see status word)    */
+    MOE_ERR_TIMEOUT = 6        /* reserved: a bounded device-side wait gave up        */
+} moe_status;
+
+/* Weight formats (GGUF-style blocks; see moe_pack_weights for the bytes). */
+typedef enum {
+    MOE_F32 = 0,    /* plain fp32 (router only)                                   */
+    MOE_Q8_0 = 1,   /* 32 weights: f16 d, i8 q[32]               w = d*q   (34 B)  */
+    MOE_Q4_K = 2,   /* 256 weights: f16 d, f16 dmin, 6-bit sc/m x 8, 4-bit q (144 B) */
+    MOE_Q2_K = 3,   /* 256 weights: 4-bit sc/m x 16, 2-bit q, f16 d, f16 dmin (84 B) */
+    MOE_MXFP4 = 4   /* 32 weights: E8M0 scale e, FP4 E2M1 q[32]  w = 2^(e-127)*q (17 B) */
+} moe_qtype;
+
+typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID = 1 } moe_gating;
+
+/* Device status word bits (moe_read_device_status). */
+#define MOE_DEV_BAD_ID 0x1u       /* an expert id outside [0, E): that slot was skipped     */
+#define MOE_DEV_DUP_ID 0x2u       /* an id repeated within one token: the repeat was skipped */
+
+/* Limits of this build. */
+#define MOE_MAX_TOKENS 16          /* T per call (small-batch decode)        */
+#define MOE_MAX_K 32               /* top-k                                  */
+#define MOE_MAX_EXPERTS 1024       /* E                                      */
+
+/* ------------------------------------------------------------------ sizes */
+
+/* Activation quantisation block for a width n: 256 if n % 256 == 0, 32 if
+ * n % 32 == 0 (the README's "multiple of 32 but not 256 -> q8_0" rule),
+ * else 0 (unsupported). */
+int moe_act_block(int n);
+
+/* Bytes of one token's q8 activation record of width n (a multiple of 16):
+ *   offset 0          : float d[n/B]        block scales, B = moe_act_block(n)
+ *   offset A          : int8  q[n]          codes, A = 16-aligned 4*n/B
+ *   offset A + n      : int16 bsum[n/16]    sum of each 16 consecutive codes
+ * T tokens are T records back to back.  Returns 0 if n is unsupported. */
+size_t moe_q8_row_bytes(int n);
+
+/* Bytes of a packed weight matrix (rows x cols), 0 if unsupported.
+ * rows % 32 == 0; cols % 256 == 0 for Q4_K, Q2_K and Q8_0; cols % 32 == 0 for
+ * MXFP4.  The packed size equals the GGUF size except for MXFP4 matrices whose
+ * cols/32 is not a multiple of 8 (a few pad bytes per 32 rows). */
+size_t moe_packed_bytes(moe_qtype qtype, int rows, int cols);
+
+/* ------------------------------------------------------------- one-time pack */
+
+/*
+ * Lossless re-layout of a row-major matrix of GGUF-style blocks (device,
+ * rows x cols/QK blocks, QK = 256 or 32) into the packed layout the FFN
+ * kernels stream with 128-bit coalesced loads (device, moe_packed_bytes).
+ * Same bits per weight; run once at load time.  This mirrors the README's
+ * load-time tensor transforms (K-quant dense tensors are requantised when
+ * loaded); here nothing is requantised, only moved.
+ *
+ * Packed layout: rows are cut into tiles of 32; a tile is a sequence of
+ * records along the columns; a record is a set of 512-byte planes, plane p
+ * holding 16 bytes for each of the 32 rows (row r of the tile at byte 16*r):
+ *   Q4_K  : record = 1 block (256 cols); planes 0..8 = the block's bytes
+ *           [16p, 16p+16) (plane 0: d, dmin, scales; 1..8: qs).      4608 B
+ *   Q2_K  : record = 1 block; planes 0..4 = bytes [16p, 16p+16) (scales,
+ *           qs), then one 128-byte plane of {d, dmin} (4 B per row). 2688 B
+ *   Q8_0  : record = 8 blocks (256 cols); planes 2b, 2b+1 = q of block b,
+ *           plane 16 = the 8 f16 d of the row.                       8704 B
+ *   MXFP4 : record = nb <= 8 blocks (the last record of a row takes the
+ *           remainder); planes 0..nb-1 = qs of block b, then a 256-byte
+ *           plane of 8 scale bytes per row (unused bytes zero). nb*512+256 B
+ * Errors: MOE_ERR_UNSUPPORTED for F32 or shapes outside the rules above.
+ */
+moe_status moe_pack_weights(const void *blocks, moe_qtype qtype, int rows, int cols,
+                            void *packed, cudaStream_t stream);
+
+/* ---------------------------------------------------------- hot-path calls */
+
+/*
+ * Activation quantisation (README "MoE resolve": activations quantised to
+ * q8_0/q8_K before integer dots).  x: device fp32 [T][n]; xq: device, T
+ * records of moe_q8_row_bytes(n), 16-byte aligned.  Per block of
+ * B = moe_act_block(n): amax = max|x|, d = amax/127, q = rint(x*(127/amax))
+ * (round half to even; IEEE division), d = 0 and q = 0 for an all-zero
+ * block; bsum = sums of 16 codes.  T in [0, MOE_MAX_TOKENS*64]; T == 0 is a
+ * no-op.
+ */
+moe_status moe_quantize_q8K(const float *x, int T, int n, void *xq, cudaStream_t stream);
+
+/*
+ * Router GEMV + top-k + gating (README intro: the router stays resident;
+ * model table: softmax and sigmoid-gated routers, top-k of E).
+ *   hidden      : device fp32 [T][H]   (read by an F32 router)
+ *   xq          : device q8 records of hidden (moe_quantize_q8K), required
+ *                 for a Q8_0 router, ignored (may be NULL) for F32
+ *   w_router    : device, F32 [E][H] row-major, or Q8_0 blocks [E][H/32]
+ *                 (GGUF row-major, not packed; rows must be 16-byte aligned,
+ *                 i.e. (H/32) % 8 == 0)
+ *   router_bias : device fp32 [E] added to the logits, or NULL
+ *   ids         : device int32 [T][k] out: the k largest logits, largest
+ *                 first, the lower index first on equal logits
+ *   weights     : device fp32 [T][k] out.  Softmax: exp(l - lmax) over the
+ *                 chosen k, normalised to sum 1 (renormalize != 0) or over all
+ *                 E (renormalize == 0).  Sigmoid: s = 1/(1+exp(-l)), divided
+ *                 by the sum over the chosen k when renormalize != 0.
+ *   logits_out  : device fp32 [T][E] out, or NULL
+ *   ws          : device workspace of moe_route_workspace_bytes(T, E) bytes,
+ *                 zero-filled before its first use; every completed call
+ *                 leaves it ready for the next one
+ * Logits are fp32 in one fixed summation order, so ids are reproducible bit
+ * for bit: the row is cut into 1024-element segments; in a segment, lane l of
+ * 32 accumulates float4 chunks l, l+32, ... with fused multiply-adds in
+ * element order; the 32 lane values are combined by an xor butterfly
+ * (offsets 16, 8, 4, 2, 1); segment values are added in order, then the bias.
+ * A Q8_0 router uses 32-block segments with lane l taking block l of the
+ * segment, value (d_w*d_x)*isum.
+ * Limits: 1 <= k <= min(E, MOE_MAX_K), E <= MOE_MAX_EXPERTS, T <= MOE_MAX_TOKENS,
+ * H % 32 == 0.
+ */
+moe_status moe_route(const float *hidden, const void *xq, int T, int H,
+                     const void *w_router, moe_qtype rtype, int E, const float *router_bias,
+                     int k, moe_gating gating, int renormalize,
+                     int32_t *ids, float *weights, float *logits_out,
+                     void *ws, size_t ws_bytes, cudaStream_t stream);
+size_t moe_route_workspace_bytes(int T, int E, int H);
+
+/* One expert: packed device matrices (moe_pack_weights) and optional biases. */
+typedef struct {
+    const void *gate;     /* packed [I][H]; NULL: this expert is not owned here  */
+    const void *up;       /* packed [I][H]                                        */
+    const void *down;     /* packed [H][I]                                        */
+    const float *b_gate;  /* device fp32 [I] or NULL                              */
+    const float *b_up;    /* device fp32 [I] or NULL                              */
+    const float *b_down;  /* device fp32 [H] or NULL (scaled by the routing weight) */
+} moe_expert;
+
+/* A set of experts of one format.  `experts` is a DEVICE array of E entries
+ * (the per-expert pointer table stays on the device; the host never walks it). */
+typedef struct {
+    moe_qtype qtype;
+    int H, I, E;
+    const moe_expert *experts;
+} moe_pool;
+
+/*
+ * Routed + shared expert FFN for T tokens (README "MoE resolve": integer
+ * dots on q8 activations with per-block rescale; SwiGLU; per-slot weighted
+ * sum; shared expert always on).
+ *   xq      : device q8 records of the T hidden states (width pool->H)
+ *   ids     : device int32 [T][k]; weights: device fp32 [T][k]
+ *   pool    : host pointer to the routed pool (qtype Q8_0, Q4_K, Q2_K or MXFP4)
+ *   shared  : host pointer to a pool with E == 1 (weight 1, no biases read),
+ *             or NULL
+ *   y       : device fp32 [T][H] out, overwritten:
+ *             y[t] = sum over slots s in slot order of w[t][s]*o(ids[t][s])
+ *                    + o_shared (added last),
+ *             o = W_down . q8(h) + b_down,  h = silu(g) * u,
+ *             g = W_gate . xq + b_gate, u = W_up . xq + b_up (fp32 h is
+ *             requantised with the moe_quantize_q8K rule, width I).
+ *             Slots whose expert is not owned (gate == NULL) add nothing: an
+ *             expert-parallel rank passes a pool with its non-owned entries
+ *             NULL and receives a partial y.
+ *   ws      : device workspace of moe_ffn_workspace_bytes() bytes, zero-filled
+ *             before its first use.  The first 4 bytes are the device status
+ *             word (MOE_DEV_* bits): an id outside [0, E) or repeated within a
+ *             token is skipped and flagged there, without failing the call.
+ * Every token's result is computed with the same arithmetic and order
+ * whatever the other tokens of the batch, so a token's y is bit-identical
+ * between T = 1 and any batch that contains it.
+ * Limits: T <= MOE_MAX_TOKENS, k <= MOE_MAX_K, E <= MOE_MAX_EXPERTS;
+ * H and I multiples of 32 (of 256 for Q4_K, Q2_K, Q8_0).
+ */
+moe_status moe_expert_ffn(const void *xq, int T, const int32_t *ids, const float *weights, int k,
+                          const moe_pool *pool, const moe_pool *shared, float *y,
+                          void *ws, size_t ws_bytes, cudaStream_t stream);
+size_t moe_ffn_workspace_bytes(int T, int k, const moe_pool *pool, const moe_pool *shared);
+
+/*
+ * Reads (and, if clear != 0, zeroes) the device status word at the start of
+ * an FFN workspace.  Synchronises `stream`.  *flags receives MOE_DEV_* bits.
+ * Returns MOE_ERR_DEVICE_STATUS if any bit was set, MOE_OK otherwise.
+ */
+moe_status moe_read_device_status(void *ws, int clear, uint32_t *flags, cudaStream_t stream);
+
+/*
+ * Test hook: the exact int32 sub-block dots of one row of a packed matrix
+ * with one q8 activation record, computed by the same device code the FFN
+ * uses (the README's one-row GPU-vs-CPU arbiter idea).  Q4_K: 8 per
+ * 256-block; Q2_K: 16; Q8_0 and MXFP4: 1 per 32-block.
+ *   packed: device (moe_pack_weights); xq: device, one record of width cols;
+ *   isums: device int32 out, cols/256*8, cols/256*16 or cols/32 entries.
+ */
+moe_status moe_debug_row_dots(const void *packed, moe_qtype qtype, int rows, int cols, int row,
+                              const void *xq, int32_t *isums, cudaStream_t stream);
+
+const char *moe_status_str(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

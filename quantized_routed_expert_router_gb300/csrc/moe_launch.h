@@ -1,0 +1,62 @@
+// moe_launch.h - internal launcher declarations shared by the translation
+// units of the library (not part of the public C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int MAXP = MOE_MAX_TOKENS * MOE_MAX_K;   // (token, slot) pairs per call
+
+struct RouteArgs {
+    const float *hidden;
+    const uint8_t *xq;
+    const void *w;
+    const float *bias;
+    int32_t *ids;
+    float *weights;
+    float *logits_out;
+    float *partial;      // ws: [T][E][nseg]
+    unsigned *counter;   // ws
+    int T, H, E, k, nseg, gating, renorm;
+};
+
+struct FfnArgs {
+    const uint8_t *xq;           // [T] records of width H
+    const int32_t *ids;          // [T][k]
+    const float *weights;        // [T][k]
+    const moe_expert *experts;   // device [E]
+    const moe_expert *shared;    // device [1] or nullptr
+    float *y;                    // [T][H]
+    unsigned *status;            // ws
+    unsigned *counters;          // ws [MAXP + 1]
+    float *h_r;                  // ws [T*k][I]
+    float *h_s;                  // ws [T][Is]
+    uint8_t *hq_r;               // ws [T*k] records of width I
+    uint8_t *hq_s;               // ws [T] records of width Is
+    int T, k, H, I, Is, E;
+    int qtype, sqtype;
+};
+
+// workspace layout of moe_expert_ffn (offsets in bytes)
+struct FfnWs {
+    size_t status, counters, h_r, h_s, hq_r, hq_s, total;
+};
+FfnWs ffn_ws_layout(int T, int k, int H, int I, int Is);
+
+int num_sms();
+int smem_optin();
+
+cudaError_t launch_quantize(const float *x, int T, int n, uint8_t *xq, cudaStream_t s);
+cudaError_t launch_route(const RouteArgs &a, int rtype, cudaStream_t s);
+cudaError_t launch_pack(const uint8_t *src, int qtype, int rows, int cols, uint8_t *dst, cudaStream_t s);
+cudaError_t launch_row_dots(const uint8_t *packed, int qtype, int cols, int row, const uint8_t *xq,
+                            int32_t *out, cudaStream_t s);
+// returns cudaErrorInvalidConfiguration if the shape needs more shared memory than a block has
+cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t s);
+
+}  // namespace moe

@@ -54,7 +54,8 @@ def _lib():
             lib = ctypes.CDLL(_SO)
             lib.synth_matrix.restype = ctypes.c_int
             lib.synth_matrix.argtypes = [ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_float,
-                                         ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
+                                         ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,
+                                         ctypes.c_int64]
             lib.synth_encode.restype = ctypes.c_int
             lib.synth_encode.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                          ctypes.c_void_p]
@@ -78,12 +79,12 @@ def row_bytes(qtype: int, cols: int) -> int:
     return int(rb)
 
 
-def matrix(qtype: int, seed: int, stream: int, sigma: float, rows: int, cols: int) -> np.ndarray:
+def matrix(qtype: int, seed: int, stream: int, sigma: float, rows: int, cols: int, row0: int = 0) -> np.ndarray:
     """rows x cols draws of N(0, sigma^2), encoded as qtype blocks: uint8 [rows, row_bytes]
-    (F32: float32 [rows, cols])."""
+    (F32: float32 [rows, cols]).  Output row r is row row0 + r of the stream."""
     rb = row_bytes(qtype, cols)
     out = np.empty((rows, rb), dtype=np.uint8)
-    rc = _lib().synth_matrix(qtype, seed, stream, sigma, rows, cols, out.ctypes.data, _threads())
+    rc = _lib().synth_matrix(qtype, seed, stream, sigma, rows, cols, out.ctypes.data, _threads(), row0)
     if rc != 0:
         raise RuntimeError(f"synth_matrix failed ({rc})")
     return out.view(np.float32) if qtype == F32 else out
@@ -213,14 +214,10 @@ def make_layer(cfg: MoEConfig, layer: int = 0, T: int = 1, seed: int = 0,
     L = Layer(cfg, layer, T, x, router, rbias, None, None, None)
     if not with_experts:
         return L
-    rbh, rbi = row_bytes(cfg.qtype, H), row_bytes(cfg.qtype, I)
-    L.gate = np.empty((E, I, rbh), np.uint8)
-    L.up = np.empty((E, I, rbh), np.uint8)
-    L.down = np.empty((E, H, rbi), np.uint8)
-    for e in range(E):
-        L.gate[e] = matrix(cfg.qtype, seed, stream_id(c, _T_GATE, layer, e), SIG_W, I, H)
-        L.up[e] = matrix(cfg.qtype, seed, stream_id(c, _T_UP, layer, e), SIG_W, I, H)
-        L.down[e] = matrix(cfg.qtype, seed, stream_id(c, _T_DOWN, layer, e), SIG_W, H, I)
+    # expert e's matrix is rows [e*rows, (e+1)*rows) of its tensor's stream
+    L.gate = matrix(cfg.qtype, seed, stream_id(c, _T_GATE, layer), SIG_W, E * I, H).reshape(E, I, -1)
+    L.up = matrix(cfg.qtype, seed, stream_id(c, _T_UP, layer), SIG_W, E * I, H).reshape(E, I, -1)
+    L.down = matrix(cfg.qtype, seed, stream_id(c, _T_DOWN, layer), SIG_W, E * H, I).reshape(E, H, -1)
     if cfg.biases:
         L.bg = normal(seed, stream_id(c, _T_BG, layer), SIG_B, E, I)
         L.bu = normal(seed, stream_id(c, _T_BU, layer), SIG_B, E, I)

@@ -8,8 +8,9 @@
  * itself (no dots, no routing, no activation quantisation).
  *
  * Determinism: every value depends only on (seed, stream, row); thread count
- * does not matter.  The normal draw is Box-Muller with a logarithm and a
- * sine/cosine evaluated here from their power series in IEEE double
+ * does not matter.  A normal draw maps 32 random bits through an inverse-CDF
+ * table (4097 points, linear interpolation; tails end near +-3.7 sigma) that
+ * is built once from the CDF's power series by bisection in IEEE double
  * arithmetic (built with -ffp-contract=off), so x86-64 and aarch64 hosts
  * produce the same bytes.
  *
@@ -49,56 +50,53 @@ static uint64_t stream_key(uint64_t seed, uint64_t stream, uint64_t row) {
     return sm64_step(&s);
 }
 
-/* uniform in (0, 1], 53 bits */
-static inline double u01(uint64_t *s) {
-    return ((double)(sm64_step(s) >> 11) + 1.0) * (1.0 / 9007199254740992.0);
+/* Standard normal CDF by its Taylor series (IEEE double, no libm):
+ * Phi(x) = 1/2 + (1/sqrt(2 pi)) sum_n (-1)^n x^(2n+1) / (2^n n! (2n+1)).
+ * Accurate to ~1e-12 for |x| <= 4, which is all the table below needs. */
+static double det_phi(double x) {
+    double term = x, sum = x, x2 = x * x;
+    for (int n = 1; n < 200; ++n) {
+        term *= -x2 / (2.0 * n);
+        double add = term / (double)(2 * n + 1);
+        sum += add;
+        if (add < 1e-18 && add > -1e-18) break;
+    }
+    return 0.5 + 0.39894228040143267793994605993438 * sum;
 }
 
-static const double LN2 = 0.69314718055994530941723212145818;
-static const double PI_2 = 1.57079632679489661923132169163975;
+/* Inverse-CDF table at u_j = (j + 0.5) / NTAB1, j = 0..NTAB; a normal draw
+ * takes 12 bits of a uniform as the cell and 16 more as the position in it. */
+#define NTAB 4096
+#define NTAB1 (NTAB + 1)
+static float g_tab[NTAB + 1];
+static pthread_once_t g_tab_once = PTHREAD_ONCE_INIT;
 
-/* natural log for x in (0, 1]: frexp is exact; ln(m) = 2 atanh((m-1)/(m+1)) */
-static double det_log(double x) {
-    int e;
-    double m = frexp(x, &e);
-    if (m < 0.70710678118654752440) { m *= 2.0; e -= 1; }
-    double s = (m - 1.0) / (m + 1.0);
-    double s2 = s * s, t = s, sum = 0.0;
-    for (int k = 0; k < 14; ++k) { sum += t / (double)(2 * k + 1); t *= s2; }
-    return 2.0 * sum + (double)e * LN2;
+static void build_table(void) {
+    for (int j = 0; j <= NTAB; ++j) {
+        double u = ((double)j + 0.5) / (double)NTAB1, lo = -6.0, hi = 6.0;
+        for (int it = 0; it < 64; ++it) {
+            double mid = 0.5 * (lo + hi);
+            if (det_phi(mid) < u) lo = mid; else hi = mid;
+        }
+        g_tab[j] = (float)(0.5 * (lo + hi));
+    }
 }
 
-/* sin and cos of theta in [0, 2*pi) by quadrant reduction and Taylor series */
-static void det_sincos(double th, double *sn, double *cs) {
-    double qf = floor(th / PI_2 + 0.5);
-    int q = ((int)qf) & 3;
-    double r = th - qf * PI_2;
-    double r2 = r * r;
-    double s = 0.0, c = 0.0, ts = r, tc = 1.0;
-    for (int k = 0; k < 11; ++k) {
-        s += ts; c += tc;
-        ts *= -r2 / (double)((2 * k + 2) * (2 * k + 3));
-        tc *= -r2 / (double)((2 * k + 1) * (2 * k + 2));
-    }
-    switch (q) {
-        case 0: *sn = s;  *cs = c;  break;
-        case 1: *sn = c;  *cs = -s; break;
-        case 2: *sn = -s; *cs = -c; break;
-        default: *sn = -c; *cs = s; break;
-    }
+static inline float normal_from_u32(uint32_t u) {
+    uint32_t cell = u >> 20, pos = (u >> 4) & 0xFFFFu;
+    float a = g_tab[cell], b = g_tab[cell + 1];
+    return a + (b - a) * ((float)pos * (1.0f / 65536.0f));
 }
 
 /* n standard normals scaled by sigma from the (seed, stream, row) key */
 static void normal_row(uint64_t seed, uint64_t stream, uint64_t row, float sigma,
                        float *out, int64_t n) {
+    pthread_once(&g_tab_once, build_table);
     uint64_t s = stream_key(seed, stream, row);
     for (int64_t i = 0; i < n; i += 2) {
-        double u1 = u01(&s), u2 = u01(&s);
-        double r = sqrt(-2.0 * det_log(u1));
-        double sn, cs;
-        det_sincos(6.28318530717958647692528676655901 * (u2 - 0x1p-53), &sn, &cs);
-        out[i] = (float)(sigma * r * cs);
-        if (i + 1 < n) out[i + 1] = (float)(sigma * r * sn);
+        uint64_t r = sm64_step(&s);
+        out[i] = sigma * normal_from_u32((uint32_t)r);
+        if (i + 1 < n) out[i + 1] = sigma * normal_from_u32((uint32_t)(r >> 32));
     }
 }
 
@@ -312,7 +310,7 @@ int synth_encode(int qtype, const float *w, int64_t rows, int64_t cols, void *ou
 
 typedef struct {
     int qtype; uint64_t seed, stream; float sigma;
-    int64_t r0, r1, cols; void *out;
+    int64_t r0, r1, cols, row0; void *out;
 } job_t;
 
 static void *matrix_worker(void *p) {
@@ -321,16 +319,17 @@ static void *matrix_worker(void *p) {
     float *row = (float *)malloc(sizeof(float) * (size_t)j->cols);
     if (!row) return (void *)1;
     for (int64_t r = j->r0; r < j->r1; ++r) {
-        normal_row(j->seed, j->stream, (uint64_t)r, j->sigma, row, j->cols);
+        normal_row(j->seed, j->stream, (uint64_t)(r + j->row0), j->sigma, row, j->cols);
         synth_encode(j->qtype, row, 1, j->cols, (uint8_t *)j->out + r * rb);
     }
     free(row);
     return NULL;
 }
 
-/* rows x cols matrix of N(0, sigma^2) values encoded as qtype (F32: raw) */
+/* rows x cols matrix of N(0, sigma^2) values encoded as qtype (F32: raw);
+ * row r of the output is row row0 + r of the stream */
 int synth_matrix(int qtype, uint64_t seed, uint64_t stream, float sigma,
-                 int64_t rows, int64_t cols, void *out, int threads) {
+                 int64_t rows, int64_t cols, void *out, int threads, int64_t row0) {
     if (synth_row_bytes(qtype, cols) < 0 || rows < 0) return -1;
     if (threads < 1) threads = 1;
     if (threads > 256) threads = 256;
@@ -339,7 +338,8 @@ int synth_matrix(int qtype, uint64_t seed, uint64_t stream, float sigma,
     int64_t per = (rows + threads - 1) / threads;
     int started = 0, rc = 0;
     for (int t = 0; t < threads; ++t) {
-        jobs[t] = (job_t){qtype, seed, stream, sigma, t * per, (t + 1) * per < rows ? (t + 1) * per : rows, cols, out};
+        jobs[t] = (job_t){qtype, seed, stream, sigma, t * per, (t + 1) * per < rows ? (t + 1) * per : rows, cols,
+                          row0, out};
         if (jobs[t].r0 >= jobs[t].r1) continue;
         if (threads == 1) { if (matrix_worker(&jobs[t])) rc = -2; continue; }
         if (pthread_create(&th[started], NULL, matrix_worker, &jobs[t]) != 0) {
