@@ -220,6 +220,31 @@ moe_status moe_expert_ffn(const void *xq, int T, const int32_t *ids, const float
 size_t moe_ffn_workspace_bytes(int T, int k, const moe_pool *pool, const moe_pool *shared);
 
 /*
+ * moe_expert_ffn for callers that cannot allocate device memory: code bound
+ * to a device-memory plan fixed at start-up, plugin hosts that pass inputs
+ * and outputs but offer no allocator, and paths where cudaMalloc/cudaFree are
+ * not allowed because they can synchronise the device or fail under memory
+ * pressure.  The pages have no counterpart to this call; it exists for
+ * deployment.  Arguments and results are those of moe_expert_ffn, without
+ * the workspace.
+ *  - Scratch is one fixed array of 2 MiB in the library's device image, held
+ *    on every device that loads the library until the process exits.  A
+ *    shape whose moe_ffn_workspace_bytes() exceeds 2 MiB returns
+ *    MOE_ERR_WORKSPACE before anything is enqueued.
+ *  - Allocates nothing.  The first call on a device looks up the array's
+ *    device address; make that first call before any stream capture.
+ *  - Every call uses the same array and finds the previous call's contents
+ *    there (the status word and tickets are cleared by each call).  Calls
+ *    that overlap on the GPU (other streams, other host threads) race and
+ *    corrupt each other's results: order them.
+ *  - The status word lives in that array and is not reported; out-of-range
+ *    or repeated ids are still skipped.
+ */
+moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, const float *weights, int k,
+                                  const moe_pool *pool, const moe_pool *shared, float *y,
+                                  cudaStream_t stream);
+
+/*
  * Reads (and, if clear != 0, zeroes) the device status word at the start of
  * an FFN workspace.  Synchronises `stream`.  *flags receives MOE_DEV_* bits.
  * Returns MOE_ERR_DEVICE_STATUS if any bit was set, MOE_OK otherwise.

@@ -22,7 +22,7 @@ MAX_TOKENS, MAX_K, MAX_EXPERTS = 16, 32, 1024
 
 EXPORTS = ["moe_act_block", "moe_q8_row_bytes", "moe_packed_bytes", "moe_pack_weights", "moe_quantize_q8K",
            "moe_route", "moe_route_workspace_bytes", "moe_expert_ffn", "moe_ffn_workspace_bytes",
-           "moe_read_device_status", "moe_debug_row_dots", "moe_status_str"]
+           "moe_read_device_status", "moe_debug_row_dots", "moe_status_str", "moe_expert_ffn_noalloc"]
 
 _P = ctypes.c_void_p
 _lib_handle = None
@@ -71,6 +71,8 @@ def lib():
         L.moe_route_workspace_bytes.argtypes = [i, i, i]
         L.moe_expert_ffn.restype = i
         L.moe_expert_ffn.argtypes = [_P, i, _P, _P, i, ctypes.POINTER(_Pool), ctypes.POINTER(_Pool), _P, _P, sz, _P]
+        L.moe_expert_ffn_noalloc.restype = i
+        L.moe_expert_ffn_noalloc.argtypes = [_P, i, _P, _P, i, ctypes.POINTER(_Pool), ctypes.POINTER(_Pool), _P, _P]
         L.moe_ffn_workspace_bytes.restype = sz
         L.moe_ffn_workspace_bytes.argtypes = [i, i, ctypes.POINTER(_Pool), ctypes.POINTER(_Pool)]
         L.moe_read_device_status.restype = i
@@ -173,6 +175,14 @@ def moe_expert_ffn(xq, T: int, ids, weights, k: int, pool: ExpertPool, shared: E
     _check(lib().moe_expert_ffn(_ptr(xq), T, _ptr(ids), _ptr(weights), k, ctypes.byref(pool.c),
                                 ctypes.byref(shared.c) if shared is not None else None, _ptr(y), _ptr(ws),
                                 ws.numel() * ws.element_size(), _stream(stream)), "moe_expert_ffn")
+
+
+def moe_expert_ffn_noalloc(xq, T: int, ids, weights, k: int, pool: ExpertPool, shared: ExpertPool | None, y,
+                           stream=None):
+    """moe_expert_ffn with the library's fixed device scratch (no workspace, no allocation)."""
+    _check(lib().moe_expert_ffn_noalloc(_ptr(xq), T, _ptr(ids), _ptr(weights), k, ctypes.byref(pool.c),
+                                        ctypes.byref(shared.c) if shared is not None else None, _ptr(y),
+                                        _stream(stream)), "moe_expert_ffn_noalloc")
 
 
 def moe_read_device_status(ws, clear: bool = True, stream=None) -> int:

@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 SO = os.path.join(PKG, "_moe.so")
-SOURCES = ["moe_api.cu", "moe_kernels.cu", "moe_ffn.cu"]
+SOURCES = ["moe_api.cu", "moe_kernels.cu", "moe_ffn.cu", "moe_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
