@@ -45,6 +45,7 @@ def parse():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-overlap", action="store_true", help="launch layers without the overlap flag")
     return p.parse_args()
 
 
@@ -227,26 +228,35 @@ def main():
     gen_s = time.perf_counter() - t_gen
     stream = torch.cuda.Stream(device=dev)
 
-    def step(ffn_only=False, route_only=False):
+    flags = 0 if args.no_overlap else moe.LAYER_OVERLAP_PREVIOUS
+
+    def step_fused():
+        for dl in layers:
+            dl.forward_fused(flags=flags, outputs=False)
+
+    def step_three(ffn_only=False):
         for dl in layers:
             if not ffn_only:
                 dl.quantize()
                 dl.route(logits=False)
-            if not route_only:
-                dl.ffn()
+            dl.ffn()
 
     with torch.cuda.stream(stream):
-        step()                        # eager once: sets kernel attributes, fills ids
+        step_three()                  # eager once: kernel attributes, ids for the byte count
+        step_fused()
     torch.cuda.synchronize()
+    bad = [moe.moe_read_device_status(dl.ws_layer) for dl in layers]
+    if any(bad):
+        raise RuntimeError(f"device status after the first fused step: {bad}")
     bytes_l = [layer_bytes(cfg, dl, moe) for dl in layers]
     step_bytes = sum(b["total"] for b in bytes_l)
     ffn_bytes = sum(b["experts"] + b["shared"] for b in bytes_l)
 
     graphs = {}
-    for name, kw in (("step", {}), ("ffn", {"ffn_only": True}), ("route", {"route_only": True})):
+    for name, fn in (("step", step_fused), ("three", step_three), ("ffn", lambda: step_three(ffn_only=True))):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            step(**kw)
+            fn()
         graphs[name] = g
     torch.cuda.synchronize()
 
@@ -277,8 +287,12 @@ def main():
     with ClockSampler(local) as cs:
         ms = timed(graphs["step"], K, W)
     clocks = cs.summary()
-    ms_ffn = timed(graphs["ffn"], K, W)
-    ms_route = timed(graphs["route"], K, W)
+    status = [moe.moe_read_device_status(dl.ws_layer) for dl in layers]
+    if any(status):
+        raise RuntimeError(f"device status after the timed region: {status}")
+    K3 = max(3, K // 4)
+    ms_three = timed(graphs["three"], K3, W)
+    ms_ffn = timed(graphs["ffn"], K3, W)
 
     # ---- end to end through the public API: pinned H2D of every layer's input,
     # the captured public-API calls, D2H of every layer's y, per step
@@ -309,9 +323,9 @@ def main():
 
     value = world * K * L * T / (ms / 1e3)
     peak, peak_src = peaks()
-    ffn_launch_ms = ms_ffn / (K * L)
-    achieved = (ffn_bytes / L) / (ffn_launch_ms / 1e3) / 1e9
-    traffic = traffic_record(f"moe_expert_ffn:{cfg.name}")
+    launch_ms = ms / (K * L)
+    achieved = (step_bytes / L) / (launch_ms / 1e3) / 1e9
+    traffic = traffic_record(f"layer_kernel:{cfg.name}:T{T}")
     cpu = None
     if rank == 0 and not args.no_cpu and host_sample:
         import oracle
@@ -340,16 +354,19 @@ def main():
                        "hbm_frac_of_measured": step_bytes * K / (ms / 1e3) / 1e9 / peak,
                        "us_per_layer": 1e3 * ms / (K * L),
                        "bytes_per_layer": step_bytes / L, "unique_experts_per_layer": float(np.mean(uniq)),
-                       "route_us_per_layer": 1e3 * ms_route / (K * L),
-                       "ffn_us_per_layer": 1e3 * ms_ffn / (K * L),
+                       "path": "moe_layer_forward (one launch per layer)"
+                               + ("" if args.no_overlap else ", overlap flag (programmatic dependent launch)"),
+                       "three_call_us_per_layer": 1e3 * ms_three / (K3 * L),
+                       "three_call_ffn_us_per_layer": 1e3 * ms_ffn / (K3 * L),
                        "setup_s": gen_s},
-            "roofline": {"bound": "hbm", "kernel": "moe_expert_ffn (gateup_kernel + down_kernel)",
+            "roofline": {"bound": "hbm", "kernel": "layer_kernel (moe_layer_forward)",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_source": peak_src, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": ffn_bytes / L},
+                         "algorithmic_bytes_per_launch": step_bytes / L,
+                         "launch_us": 1e3 * launch_ms},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": K * L * 4,
+            "gpu_launches": K * L,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

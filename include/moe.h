@@ -65,6 +65,8 @@ typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID = 1 } moe_gating;
 /* Device status word bits (moe_read_device_status). */
 #define MOE_DEV_BAD_ID 0x1u       /* an expert id outside [0, E): that slot was skipped     */
 #define MOE_DEV_DUP_ID 0x2u       /* an id repeated within one token: the repeat was skipped */
+#define MOE_DEV_TIMEOUT 0x4u      /* a bounded wait in moe_layer_forward gave up: y is invalid,
+                                     zero the workspace before the next call */
 
 /* Limits of this build. */
 #define MOE_MAX_TOKENS 16          /* T per call (small-batch decode)        */
@@ -243,6 +245,44 @@ size_t moe_ffn_workspace_bytes(int T, int k, const moe_pool *pool, const moe_poo
 moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, const float *weights, int k,
                                   const moe_pool *pool, const moe_pool *shared, float *y,
                                   cudaStream_t stream);
+
+/*
+ * The whole layer in one launch: quantise (moe_quantize_q8K's rule), route
+ * (moe_route's fixed-order logits, top-k and gating) and the routed + shared
+ * expert FFN (moe_expert_ffn's arithmetic), for decode where the three steps
+ * sit back to back.  One persistent block per SM: every block quantises x and
+ * computes the logits of its own router rows, a device-wide ticket publishes
+ * the logits, each block selects the same top-k and streams its share of the
+ * chosen experts' packed weights with TMA bulk copies into a shared-memory
+ * ring; h and the per-tile slot sums are exchanged through the workspace with
+ * release/acquire tickets.  Results equal those of the three calls (same
+ * arithmetic and summation orders; y within rounding of moe_expert_ffn).
+ *   hidden      : device fp32 [T][H]; w_router/rtype/router_bias/k/gating/
+ *                 renormalize as in moe_route; pool/shared as in moe_expert_ffn
+ *                 (shared: the same format as pool or Q8_0)
+ *   y           : device fp32 [T][H] out
+ *   ids_out, weights_out, logits_out, xq_out: optional outputs (NULL to skip)
+ *   ws          : device workspace of moe_layer_workspace_bytes() bytes,
+ *                 zero-filled before its first use and after any call that set
+ *                 MOE_DEV_TIMEOUT; completed calls leave it ready for the next
+ *   flags       : MOE_LAYER_OVERLAP_PREVIOUS lets this launch start while the
+ *                 previous kernel in the stream is still running (programmatic
+ *                 dependent launch): before that kernel has finished, the call
+ *                 reads only weights, router and expert tables, so none of those
+ *                 may be written by the previous kernel; hidden and everything
+ *                 else are read only after it completes.
+ * Every device-side wait is bounded (0.4 s): on timeout the call sets
+ * MOE_DEV_TIMEOUT in the status word (moe_read_device_status) and returns.
+ * Limits as moe_route and moe_expert_ffn; additionally the blocks must all be
+ * resident at once (checked: MOE_ERR_UNSUPPORTED otherwise).
+ */
+#define MOE_LAYER_OVERLAP_PREVIOUS 0x1u
+moe_status moe_layer_forward(const float *hidden, int T, const void *w_router, moe_qtype rtype,
+                             const float *router_bias, int k, moe_gating gating, int renormalize,
+                             const moe_pool *pool, const moe_pool *shared, float *y,
+                             int32_t *ids_out, float *weights_out, float *logits_out, void *xq_out,
+                             void *ws, size_t ws_bytes, unsigned flags, cudaStream_t stream);
+size_t moe_layer_workspace_bytes(int T, int k, const moe_pool *pool, const moe_pool *shared);
 
 /*
  * Reads (and, if clear != 0, zeroes) the device status word at the start of

@@ -22,7 +22,10 @@ MAX_TOKENS, MAX_K, MAX_EXPERTS = 16, 32, 1024
 
 EXPORTS = ["moe_act_block", "moe_q8_row_bytes", "moe_packed_bytes", "moe_pack_weights", "moe_quantize_q8K",
            "moe_route", "moe_route_workspace_bytes", "moe_expert_ffn", "moe_ffn_workspace_bytes",
-           "moe_read_device_status", "moe_debug_row_dots", "moe_status_str", "moe_expert_ffn_noalloc"]
+           "moe_read_device_status", "moe_debug_row_dots", "moe_status_str", "moe_expert_ffn_noalloc",
+           "moe_layer_forward", "moe_layer_workspace_bytes"]
+LAYER_OVERLAP_PREVIOUS = 0x1
+DEV_TIMEOUT = 0x4
 
 _P = ctypes.c_void_p
 _lib_handle = None
@@ -73,6 +76,11 @@ def lib():
         L.moe_expert_ffn.argtypes = [_P, i, _P, _P, i, ctypes.POINTER(_Pool), ctypes.POINTER(_Pool), _P, _P, sz, _P]
         L.moe_expert_ffn_noalloc.restype = i
         L.moe_expert_ffn_noalloc.argtypes = [_P, i, _P, _P, i, ctypes.POINTER(_Pool), ctypes.POINTER(_Pool), _P, _P]
+        L.moe_layer_forward.restype = i
+        L.moe_layer_forward.argtypes = [_P, i, _P, i, _P, i, i, i, ctypes.POINTER(_Pool), ctypes.POINTER(_Pool),
+                                        _P, _P, _P, _P, _P, _P, sz, ctypes.c_uint, _P]
+        L.moe_layer_workspace_bytes.restype = sz
+        L.moe_layer_workspace_bytes.argtypes = [i, i, ctypes.POINTER(_Pool), ctypes.POINTER(_Pool)]
         L.moe_ffn_workspace_bytes.restype = sz
         L.moe_ffn_workspace_bytes.argtypes = [i, i, ctypes.POINTER(_Pool), ctypes.POINTER(_Pool)]
         L.moe_read_device_status.restype = i
@@ -183,6 +191,22 @@ def moe_expert_ffn_noalloc(xq, T: int, ids, weights, k: int, pool: ExpertPool, s
     _check(lib().moe_expert_ffn_noalloc(_ptr(xq), T, _ptr(ids), _ptr(weights), k, ctypes.byref(pool.c),
                                         ctypes.byref(shared.c) if shared is not None else None, _ptr(y),
                                         _stream(stream)), "moe_expert_ffn_noalloc")
+
+
+def moe_layer_workspace_bytes(T: int, k: int, pool: ExpertPool, shared: ExpertPool | None) -> int:
+    return lib().moe_layer_workspace_bytes(T, k, ctypes.byref(pool.c),
+                                           ctypes.byref(shared.c) if shared is not None else None)
+
+
+def moe_layer_forward(hidden, w_router, rtype: int, router_bias, k: int, gating: int, renormalize: bool,
+                      pool: ExpertPool, shared: ExpertPool | None, y, ws, ids_out=None, weights_out=None,
+                      logits_out=None, xq_out=None, flags: int = 0, T: int | None = None, stream=None):
+    T = hidden.shape[0] if T is None else T
+    _check(lib().moe_layer_forward(_ptr(hidden), T, _ptr(w_router), rtype, _ptr(router_bias), k, gating,
+                                   int(bool(renormalize)), ctypes.byref(pool.c),
+                                   ctypes.byref(shared.c) if shared is not None else None, _ptr(y),
+                                   _ptr(ids_out), _ptr(weights_out), _ptr(logits_out), _ptr(xq_out), _ptr(ws),
+                                   ws.numel() * ws.element_size(), flags, _stream(stream)), "moe_layer_forward")
 
 
 def moe_read_device_status(ws, clear: bool = True, stream=None) -> int:

@@ -106,6 +106,23 @@ __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
 
 __device__ __forceinline__ int4 lds128(const int8_t *p) { return *reinterpret_cast<const int4 *>(p); }
 
+__device__ __forceinline__ uint32_t saddr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ uint4 lds_u4(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr(p)));
+    return v;
+}
+__device__ __forceinline__ uint2 lds_u2(const void *p) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(saddr(p)));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u1(const void *p) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr(p)));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t byte_of(uint32_t w, int i) { return (w >> (8 * i)) & 0xFFu; }
 
 // ------------------------------------------------------------------ Q4_K
@@ -123,6 +140,11 @@ struct FQ4K {
 #pragma unroll
         for (int p = 0; p < 9; ++p) w.c[p] = ldg_stream(rec + p * 512 + lane * 16);
     }
+    __device__ static void load_s(W &w, const uint8_t *rec, int, int lane) {
+#pragma unroll
+        for (int p = 0; p < 9; ++p) w.c[p] = lds_u4(rec + p * 512 + lane * 16);
+    }
+    __host__ __device__ static uint32_t rec_bytes(int, int) { return REC; }
     // exact sub-block dots: is[j] = sum over the 32 elements of sub-block j
     __host__ __device__ static int rec_blocks(int, int) { return 8; }
     __device__ static void isums(const W &w, const Act &a, int k0, int, int *is) {
@@ -182,6 +204,13 @@ struct FQ2K {
         for (int p = 0; p < 4; ++p) w.q[p] = ldg_stream(rec + (1 + p) * 512 + lane * 16);
         w.dd = ldg_stream32(rec + 5 * 512 + lane * 4);
     }
+    __device__ static void load_s(W &w, const uint8_t *rec, int, int lane) {
+        w.s = lds_u4(rec + lane * 16);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) w.q[p] = lds_u4(rec + (1 + p) * 512 + lane * 16);
+        w.dd = lds_u1(rec + 5 * 512 + lane * 4);
+    }
+    __host__ __device__ static uint32_t rec_bytes(int, int) { return REC; }
     __host__ __device__ static int rec_blocks(int, int) { return 8; }
     __device__ static void isums(const W &w, const Act &a, int k0, int, int *is) {
         const int8_t *x = a.q + k0;
@@ -233,6 +262,12 @@ struct FQ80 {
         for (int p = 0; p < 16; ++p) w.q[p] = ldg_stream(rec + p * 512 + lane * 16);
         w.d = ldg_stream(rec + 16 * 512 + lane * 16);
     }
+    __device__ static void load_s(W &w, const uint8_t *rec, int, int lane) {
+#pragma unroll
+        for (int p = 0; p < 16; ++p) w.q[p] = lds_u4(rec + p * 512 + lane * 16);
+        w.d = lds_u4(rec + 16 * 512 + lane * 16);
+    }
+    __host__ __device__ static uint32_t rec_bytes(int, int) { return REC; }
     __host__ __device__ static int rec_blocks(int, int) { return 8; }
     __device__ static void isums(const W &w, const Act &a, int k0, int, int *is) {
         const int8_t *x = a.q + k0;
@@ -297,6 +332,13 @@ struct FMX4 {
             if (b < nb) w.q[b] = ldg_stream(rec + b * 512 + lane * 16);
         w.e = ldg_stream64(rec + nb * 512 + lane * 8);
     }
+    __device__ static void load_s(W &w, const uint8_t *rec, int nb, int lane) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+            if (b < nb) w.q[b] = lds_u4(rec + b * 512 + lane * 16);
+        w.e = lds_u2(rec + nb * 512 + lane * 8);
+    }
+    __host__ __device__ static uint32_t rec_bytes(int cols, int r) { return (uint32_t)rec_blocks(cols, r) * 512 + 256; }
     // magnitudes 0,1,2,3 | 4,6,8,12 of the doubled E2M1 lattice
     static constexpr uint32_t LUT0 = 0x03020100u, LUT1 = 0x0C080604u;
     // codes of one 32-block: is = sum v_i * x_i; x points at the block's codes

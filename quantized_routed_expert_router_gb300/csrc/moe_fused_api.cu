@@ -1,0 +1,195 @@
+// moe_fused_api.cu - moe_layer_forward: validation, workspace and shared
+// memory planning, dispatch of the fused layer kernel (moe_fused.cuh).
+#include "moe_common.cuh"
+#include "moe_launch.h"
+
+namespace moe {
+
+cudaError_t launch_layer_q4k(const LayerArgs &a, int sqtype, int G, size_t smem, bool pdl, cudaStream_t s);
+cudaError_t launch_layer_q2k(const LayerArgs &a, int sqtype, int G, size_t smem, bool pdl, cudaStream_t s);
+cudaError_t launch_layer_q80(const LayerArgs &a, int sqtype, int G, size_t smem, bool pdl, cudaStream_t s);
+cudaError_t launch_layer_mx4(const LayerArgs &a, int sqtype, int G, size_t smem, bool pdl, cudaStream_t s);
+
+// constants mirrored from moe_fused.cuh (kept in one place there; checked below)
+constexpr int kLW = 8, kNBAR = 32;
+constexpr uint32_t kRingDefault = 80 * 1024;
+
+static size_t al16(size_t v) { return (v + 15) & ~(size_t)15; }
+
+LayerWs layer_ws_layout(int T, int k, int H, int I, int Is, int E) {
+    auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    const size_t P = (size_t)T * k;
+    LayerWs w;
+    w.status = 0;
+    w.route_ctr = 64;
+    w.done_ctr = 128;
+    w.hctr = 256;
+    w.yticket = al(w.hctr + 4 * (size_t)(MAXP + 1));
+    w.logits = al(w.yticket + 4 * (size_t)(H / 32));
+    w.h_r = al(w.logits + 4 * (size_t)T * E);
+    w.h_s = al(w.h_r + 4 * P * I);
+    w.o_r = al(w.h_s + 4 * (size_t)T * (Is > 0 ? Is : 0));
+    w.o_s = al(w.o_r + 4 * P * H);
+    w.total = al(w.o_s + 4 * (size_t)T * H);
+    return w;
+}
+
+// largest ring item of a format: a gate+up record pair, or one down record
+static uint32_t max_item(int q, int H, int I) {
+    auto rec = [](int qq, int cols) -> uint32_t {
+        switch (qq) {
+            case MOE_Q4_K: return 9 * 512;
+            case MOE_Q2_K: return 5 * 512 + 128;
+            case MOE_Q8_0: return 17 * 512;
+            default: {
+                const int nb = cols / 32 < 8 ? cols / 32 : 8;
+                return (uint32_t)nb * 512 + 256;
+            }
+        }
+    };
+    const uint32_t a = 2 * rec(q, H), b = rec(q, I);
+    return a > b ? a : b;
+}
+
+cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStream_t s) {
+    int G = num_sms();
+    if (G > 256) G = 256;
+    const int nseg = (a.H + 1023) / 1024;
+    const int rr = (a.E + G - 1) / G;   // router rows per block, at most
+    const size_t rowb = a.rtype == MOE_F32 ? (size_t)a.H * 4 : (size_t)(a.H / 32) * 34;
+    uint32_t item = max_item(qtype, a.H, a.I);
+    if (a.shared) {
+        const uint32_t si = max_item(sqtype, a.H, a.Is);
+        if (si > item) item = si;
+    }
+    a.table_in_smem = (size_t)a.E * sizeof(moe_expert) <= 16 * 1024 ? 1 : 0;
+    a.xrec = q8_row_bytes(a.H);
+    const int Imax = a.Is > a.I ? a.Is : a.I;
+    a.hrec = q8_row_bytes(Imax);
+    a.NT = a.T <= 1 ? 1 : (a.T <= 4 ? 4 : 16);
+
+    Smem o;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = al16(off + bytes);
+        return (uint32_t)at;
+    };
+    const size_t fixed_router = (size_t)rr * rowb;
+    const size_t fixed_rest = (2 * kNBAR + 1) * 8 + kNBAR * 4 + fixed_router +
+                              (a.table_in_smem ? a.E * sizeof(moe_expert) : 0) + a.T * a.xrec + a.T * a.hrec +
+                              4 * (size_t)a.T * a.E + 4 * (size_t)rr * nseg * a.T + 8 * (size_t)a.P +
+                              4 * (5 * (size_t)a.P + 1) + 2 * kLW * 2 * a.NT * 32 * 4 + 2048 + 16 * 16;
+    const size_t optin = (size_t)smem_optin();
+    if (fixed_rest + 2 * (size_t)item > optin) return cudaErrorInvalidConfiguration;
+    size_t ring = kRingDefault;
+    if (ring < 2 * (size_t)item) ring = 2 * (size_t)item;
+    if (fixed_rest + ring > optin) ring = (optin - fixed_rest) & ~(size_t)127;
+    a.ring_bytes = (uint32_t)ring;
+    o.ring = take(ring);
+    o.bars = take((2 * kNBAR + 1) * 8);
+    o.starts = take(kNBAR * 4);
+    o.router = take(fixed_router);
+    o.table = take(a.table_in_smem ? a.E * sizeof(moe_expert) : 0);
+    o.xq = take(a.T * a.xrec);
+    o.hq = take(a.T * a.hrec);
+    o.lg = take(4 * (size_t)a.T * a.E);
+    o.segv = take(4 * (size_t)rr * nseg * a.T);
+    o.ids = take(4 * (size_t)a.P);
+    o.wts = take(4 * (size_t)a.P);
+    o.grp = take(4 * (5 * (size_t)a.P + 1));
+    o.red = take(2 * kLW * 2 * a.NT * 32 * 4);
+    o.misc = take(2048);
+    o.total = (uint32_t)off;
+    if (o.total > optin) return cudaErrorInvalidConfiguration;
+    a.sm = o;
+    switch (qtype) {
+        case MOE_Q4_K: return launch_layer_q4k(a, sqtype, G, o.total, pdl, s);
+        case MOE_Q2_K: return launch_layer_q2k(a, sqtype, G, o.total, pdl, s);
+        case MOE_Q8_0: return launch_layer_q80(a, sqtype, G, o.total, pdl, s);
+        case MOE_MXFP4: return launch_layer_mx4(a, sqtype, G, o.total, pdl, s);
+    }
+    return cudaErrorNotSupported;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+bool al16p(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool fmt_ok(int q) { return q == MOE_Q8_0 || q == MOE_Q4_K || q == MOE_Q2_K || q == MOE_MXFP4; }
+bool cols_ok(int q, int cols) { return cols > 0 && (q == MOE_MXFP4 ? cols % 32 == 0 : cols % 256 == 0); }
+}  // namespace
+
+extern "C" {
+
+size_t moe_layer_workspace_bytes(int T, int k, const moe_pool *pool, const moe_pool *shared) {
+    if (T < 1 || k < 1 || !pool) return 0;
+    return layer_ws_layout(T, k, pool->H, pool->I, shared ? shared->I : 0, pool->E).total;
+}
+
+moe_status moe_layer_forward(const float *hidden, int T, const void *w_router, moe_qtype rtype,
+                             const float *router_bias, int k, moe_gating gating, int renormalize,
+                             const moe_pool *pool, const moe_pool *shared, float *y, int32_t *ids_out,
+                             float *weights_out, float *logits_out, void *xq_out, void *ws, size_t ws_bytes,
+                             unsigned flags, cudaStream_t stream) {
+    if (T < 0 || T > MOE_MAX_TOKENS || k < 1 || k > MOE_MAX_K) return MOE_ERR_INVALID_ARG;
+    if (!pool || !pool->experts || !fmt_ok(pool->qtype)) return MOE_ERR_INVALID_ARG;
+    const int H = pool->H, I = pool->I, E = pool->E;
+    if (H <= 0 || I <= 0 || H % 32 || I % 32 || E < 1 || E > MOE_MAX_EXPERTS || k > E) return MOE_ERR_INVALID_ARG;
+    if (gating != MOE_GATE_SOFTMAX && gating != MOE_GATE_SIGMOID) return MOE_ERR_INVALID_ARG;
+    if (shared && (!shared->experts || shared->E != 1 || !fmt_ok(shared->qtype) || shared->I <= 0 ||
+                   shared->I % 32 || shared->H != H))
+        return MOE_ERR_INVALID_ARG;
+    if (rtype != MOE_F32 && rtype != MOE_Q8_0) return MOE_ERR_UNSUPPORTED;
+    if (rtype == MOE_Q8_0 && H % 256) return MOE_ERR_UNSUPPORTED;
+    if (!cols_ok(pool->qtype, H) || !cols_ok(pool->qtype, I)) return MOE_ERR_UNSUPPORTED;
+    if (shared && (!cols_ok(shared->qtype, H) || !cols_ok(shared->qtype, shared->I))) return MOE_ERR_UNSUPPORTED;
+    if (shared && shared->qtype != pool->qtype && shared->qtype != MOE_Q8_0) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!hidden || !w_router || !y || !al16p(hidden) || !al16p(w_router) || !al16p(y)) return MOE_ERR_INVALID_ARG;
+    if (xq_out && !al16p(xq_out)) return MOE_ERR_INVALID_ARG;
+    const LayerWs L = layer_ws_layout(T, k, H, I, shared ? shared->I : 0, E);
+    if (!ws || ws_bytes < L.total || !al16p(ws)) return MOE_ERR_WORKSPACE;
+    char *w = (char *)ws;
+    LayerArgs a = {};
+    a.x = hidden;
+    a.w_router = w_router;
+    a.rbias = router_bias;
+    a.experts = pool->experts;
+    a.shared = shared ? shared->experts : nullptr;
+    a.y = y;
+    a.ids_out = ids_out;
+    a.w_out = weights_out;
+    a.logits_out = logits_out;
+    a.xq_out = (uint8_t *)xq_out;
+    a.status = (unsigned *)(w + L.status);
+    a.route_ctr = (unsigned *)(w + L.route_ctr);
+    a.done_ctr = (unsigned *)(w + L.done_ctr);
+    a.hctr = (unsigned *)(w + L.hctr);
+    a.yticket = (unsigned *)(w + L.yticket);
+    a.logits = (float *)(w + L.logits);
+    a.h_r = (float *)(w + L.h_r);
+    a.h_s = (float *)(w + L.h_s);
+    a.o_r = (float *)(w + L.o_r);
+    a.o_s = (float *)(w + L.o_s);
+    a.rtype = rtype;
+    a.k = k;
+    a.gating = gating;
+    a.renorm = renormalize ? 1 : 0;
+    a.T = T;
+    a.H = H;
+    a.I = I;
+    a.Is = shared ? shared->I : 0;
+    a.E = E;
+    a.P = T * k;
+    const cudaError_t e =
+        launch_layer(a, pool->qtype, shared ? shared->qtype : pool->qtype, (flags & MOE_LAYER_OVERLAP_PREVIOUS) != 0,
+                     stream);
+    if (e == cudaSuccess) return MOE_OK;
+    if (e == cudaErrorInvalidConfiguration || e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+    return MOE_ERR_CUDA;
+}
+
+}  // extern "C"

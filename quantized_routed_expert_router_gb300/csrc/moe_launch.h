@@ -42,6 +42,39 @@ struct FfnArgs {
     int qtype, sqtype;
 };
 
+// fused layer kernel: shared-memory carve-up (byte offsets) and arguments
+struct Smem {
+    uint32_t ring, bars, starts, router, table, xq, hq, lg, segv, ids, wts, grp, red, misc, total;
+};
+
+struct LayerArgs {
+    const float *x;                 // [T][H]
+    const void *w_router;
+    const float *rbias;
+    const moe_expert *experts;      // device [E]
+    const moe_expert *shared;       // device [1] or nullptr
+    float *y;                       // [T][H]
+    int32_t *ids_out;               // optional outputs
+    float *w_out;
+    float *logits_out;
+    uint8_t *xq_out;
+    unsigned *status, *route_ctr, *done_ctr, *hctr, *yticket;   // workspace
+    float *logits, *h_r, *h_s, *o_r, *o_s;
+    int rtype, k, gating, renorm;
+    int T, H, I, Is, E, P, NT;
+    int table_in_smem;
+    uint32_t ring_bytes;
+    size_t xrec, hrec;
+    Smem sm;
+};
+
+struct LayerWs {
+    size_t status, route_ctr, done_ctr, hctr, yticket, logits, h_r, h_s, o_r, o_s, total;
+};
+LayerWs layer_ws_layout(int T, int k, int H, int I, int Is, int E);
+// plans shared memory and launches the fused layer kernel for the pool's formats
+cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStream_t s);
+
 // workspace layout of moe_expert_ffn (offsets in bytes)
 struct FfnWs {
     size_t status, counters, h_r, h_s, hq_r, hq_s, total;

@@ -10,8 +10,8 @@ import numpy as np
 import torch
 
 from . import (ExpertPool, F32, SIGMOID, SOFTMAX, device_bytes, moe_expert_ffn, moe_ffn_workspace_bytes,
-               moe_pack_weights, moe_packed_bytes, moe_q8_row_bytes, moe_quantize_q8K, moe_route,
-               moe_route_workspace_bytes)
+               moe_layer_forward, moe_layer_workspace_bytes, moe_pack_weights, moe_packed_bytes,
+               moe_q8_row_bytes, moe_quantize_q8K, moe_route, moe_route_workspace_bytes)
 
 
 def _dev(a, device, dtype=None):
@@ -86,6 +86,8 @@ class DeviceLayer:
         self.ws_route = torch.zeros(moe_route_workspace_bytes(T, self.E, self.H), dtype=torch.uint8, device=d)
         self.ws_ffn = torch.zeros(moe_ffn_workspace_bytes(T, self.k, self.pool, self.shared), dtype=torch.uint8,
                                   device=d)
+        self.ws_layer = torch.zeros(moe_layer_workspace_bytes(T, self.k, self.pool, self.shared),
+                                    dtype=torch.uint8, device=d)
 
     def quantize(self, x=None, stream=None):
         moe_quantize_q8K(self.x if x is None else x, self.xq, stream)
@@ -102,7 +104,19 @@ class DeviceLayer:
                        self.y if y is None else y, self.ws_ffn, stream)
 
     def forward(self, x=None, stream=None, logits=True):
+        """three calls: moe_quantize_q8K, moe_route, moe_expert_ffn"""
         self.quantize(x, stream)
         self.route(x, stream, logits)
         self.ffn(stream=stream)
+        return self.y
+
+    def forward_fused(self, x=None, stream=None, outputs=True, flags=0, pool=None, shared="default", y=None):
+        """one call: moe_layer_forward"""
+        x = self.x if x is None else x
+        moe_layer_forward(x, self.router, self.router_qtype, self.router_bias, self.k, self.gating, self.renorm,
+                          self.pool if pool is None else pool, self.shared if shared == "default" else shared,
+                          self.y if y is None else y, self.ws_layer,
+                          ids_out=self.ids if outputs else None, weights_out=self.w if outputs else None,
+                          logits_out=self.logits if outputs else None, xq_out=self.xq if outputs else None,
+                          flags=flags, stream=stream)
         return self.y

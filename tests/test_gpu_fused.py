@@ -1,0 +1,90 @@
+"""moe_layer_forward (one launch per layer) against the CPU oracle and against
+the three-call path (quantise, route, expert FFN) through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import assert_y_close, unpack_q8_records
+
+pytestmark = pytest.mark.gpu
+
+moe = pytest.importorskip("quantized_routed_expert_router_gb300")
+from quantized_routed_expert_router_gb300.device_layer import DeviceLayer  # noqa: E402
+
+SMALL = {
+    "tiny q8_0": (synth.shrink(synth.CONFIGS["tiny"], E=6), 3),
+    "a3b q4_K + shared": (synth.shrink(synth.CONFIGS["a3b"], H=1024, I=512, E=16, k=4, shared_I=256), 3),
+    "oss20b mxfp4 + biases, ragged records": (synth.shrink(synth.CONFIGS["oss20b"], H=2880, I=320, E=6, k=3), 4),
+    "wide q2_K + q8_0 shared, q8_0 router": (synth.shrink(synth.CONFIGS["wide"], H=1536, I=512, E=12, k=4,
+                                                          shared_I=512), 2),
+    "a22b q4_K T=16 zipf": (synth.shrink(synth.CONFIGS["a22b"], H=1024, I=768, E=24, k=4), 16),
+    "a22b q4_K T=1": (synth.shrink(synth.CONFIGS["a22b"], H=1024, I=768, E=24, k=4), 1),
+}
+
+
+def np_(t):
+    return t.detach().cpu().numpy()
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("flags", [0, 1])
+def test_fused_layer_parity(name, flags):
+    cfg, T = SMALL[name]
+    L = synth.make_layer(cfg, 0, T=T, zipf=(T == 16))
+    ref = oracle.layer_forward(L)
+    dl = DeviceLayer(L, "cuda")
+    dl.forward()                                   # three-call path
+    torch.cuda.synchronize()
+    y3 = np_(dl.y).copy()
+    for rep in range(3):                           # tickets must rearm between calls
+        dl.y.fill_(float("nan"))
+        dl.ids.fill_(-1)
+        dl.forward_fused(flags=flags)
+        torch.cuda.synchronize()
+        assert moe.moe_read_device_status(dl.ws_layer) == 0
+        assert np.array_equal(np_(dl.ids), ref["ids"])
+        assert np.array_equal(np_(dl.logits), ref["logits"])
+        assert np.allclose(np_(dl.w), ref["w"], rtol=1e-6, atol=1e-7)
+        for g, w in zip(unpack_q8_records(np_(dl.xq), T, cfg.H), ref["xq"]):
+            assert np.array_equal(g, w)
+        assert_y_close(np_(dl.y), ref["y"], name)
+        # same arithmetic and summation order as the three calls
+        assert np.array_equal(np_(dl.y), y3), rep
+
+
+def test_fused_ownership_partition():
+    cfg = synth.shrink(synth.CONFIGS["wide"], H=1024, I=512, E=16, k=4, shared_I=256)
+    L = synth.make_layer(cfg, 0, T=3)
+    ref = oracle.layer_forward(L)
+    dl = DeviceLayer(L, "cuda")
+    own = np.arange(cfg.E) % 3 == 0
+    ys = []
+    for mask, sh in ((own, True), (~own, False)):
+        y = torch.empty_like(dl.y)
+        dl.forward_fused(pool=dl.make_pool(mask), shared=dl.shared if sh else None, y=y)
+        torch.cuda.synchronize()
+        ys.append(np_(y).astype(np.float64))
+        assert_y_close(ys[-1], oracle.expert_ffn(L, ref["xq"], ref["ids"], ref["w"], owned=mask, shared=sh)["y"],
+                       "partial")
+    assert_y_close(ys[0] + ys[1], ref["y"], "sum of partials")
+    # nothing owned and no shared expert: y = 0
+    y = torch.full_like(dl.y, 7.0)
+    dl.forward_fused(pool=dl.make_pool(np.zeros(cfg.E, bool)), shared=None, y=y)
+    torch.cuda.synchronize()
+    assert not np_(y).any()
+
+
+def test_fused_back_to_back_layers_with_overlap():
+    """a stack of distinct layers launched back to back with the overlap flag"""
+    cfg = synth.shrink(synth.CONFIGS["a3b"], H=1024, I=512, E=32, k=4, shared_I=256)
+    layers = [synth.make_layer(cfg, l, T=1) for l in range(6)]
+    dls = [DeviceLayer(L, "cuda") for L in layers]
+    for _ in range(2):
+        for dl in dls:
+            dl.forward_fused(flags=moe.LAYER_OVERLAP_PREVIOUS, outputs=False)
+        torch.cuda.synchronize()
+        for L, dl in zip(layers, dls):
+            assert moe.moe_read_device_status(dl.ws_layer) == 0
+            assert_y_close(np_(dl.y), oracle.layer_forward(L)["y"], f"layer {L.layer}")
