@@ -271,7 +271,7 @@ moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, con
  *                 reads only weights, router and expert tables, so none of those
  *                 may be written by the previous kernel; hidden and everything
  *                 else are read only after it completes.
- * Every device-side wait is bounded (0.4 s): on timeout the call sets
+ * Every device-side wait is bounded (8e8 SM cycles, under a second): on timeout the call sets
  * MOE_DEV_TIMEOUT in the status word (moe_read_device_status) and returns.
  * Limits as moe_route and moe_expert_ffn; additionally the blocks must all be
  * resident at once (checked: MOE_ERR_UNSUPPORTED otherwise).

@@ -134,9 +134,9 @@ __device__ void gateup_dots(const uint8_t *gtile, const uint8_t *utile, int H, i
                 const Act x = act_view(xs + i * xrec, H);
                 int is[F::NSUB];
                 F::isums(wg, x, k0, nb, is);
-                ag[i] += F::combine(wg, x, k0, nb, is);
+                ag[i] = __fadd_rn(ag[i], F::combine(wg, x, k0, nb, is));
                 F::isums(wu, x, k0, nb, is);
-                au[i] += F::combine(wu, x, k0, nb, is);
+                au[i] = __fadd_rn(au[i], F::combine(wu, x, k0, nb, is));
             }
         }
     }

@@ -28,7 +28,7 @@
 //     its expert, requantises that expert's h locally, and ends with o rows
 //     plus a ticket on its row tile; the block that completes a row tile sums
 //     the slots of each token in slot order (shared expert last) into y.
-//  Every wait is bounded by the global timer; a timeout sets MOE_DEV_TIMEOUT,
+//  Every wait is bounded (SM cycle counter); a timeout sets MOE_DEV_TIMEOUT,
 //  drains this block's copies in flight and returns.
 #pragma once
 
@@ -40,7 +40,9 @@ namespace moe {
 constexpr int LW = 8;                  // consumer warps
 constexpr int LT = (LW + 1) * 32;      // threads per block (with the producer warp)
 constexpr int NBAR = 32;               // ring items in flight (barrier slots)
-constexpr unsigned long long WAIT_NS = 400ull * 1000ull * 1000ull;   // 0.4 s per wait
+// bound on every device-side wait, in SM clock cycles (about 0.4-1 s at the
+// clocks this part runs at); the cycle counter is cheap to poll
+constexpr long long WAIT_CYCLES = 800ll * 1000ll * 1000ll;
 
 // ------------------------------------------------------------ PTX helpers
 
@@ -70,9 +72,9 @@ __device__ __forceinline__ bool mbar_test(uint64_t *b, uint32_t parity) {
 // bounded wait on an mbarrier phase; false on timeout
 __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity) {
     if (mbar_test(b, parity)) return true;
-    const unsigned long long t0 = gtimer();
+    const long long t0 = clock64();
     while (!mbar_test(b, parity))
-        if (gtimer() - t0 > WAIT_NS) return false;
+        if (clock64() - t0 > WAIT_CYCLES) return false;
     return true;
 }
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -100,9 +102,9 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
 // bounded spin until *p >= target; false on timeout
 __device__ __forceinline__ bool spin_geq(const unsigned *p, unsigned target) {
     if (ld_acquire(p) >= target) return true;
-    const unsigned long long t0 = gtimer();
+    const long long t0 = clock64();
     while (ld_acquire(p) < target)
-        if (gtimer() - t0 > WAIT_NS) return false;
+        if (clock64() - t0 > WAIT_CYCLES) return false;
     return true;
 }
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }   // consumers only
@@ -113,12 +115,28 @@ struct Misc {
     volatile int abort;
     int U, n_sa, n_ra, nA, n_sb, n_rb, nB, jb0, jb1;
     int tilesI, tilesIs, tilesH;
-    int hq_key;          // expert whose h is requantised in hq (-1 none, MAXP shared)
     int nc;              // contributions per row tile of y
     uint32_t bitmap[MOE_MAX_EXPERTS / 32];
     int wpre[MOE_MAX_EXPERTS / 32];
-    double bsum[LW];
+    uint32_t ytiles[8];  // row tiles of H this block contributed to (H <= 8192)
+    int hpend[MAXP + 1]; // h tiles this block wrote per expert, not yet released
+    int nkeys, kkey[64], kslot[64];   // experts of the current B batch and their hq slots
+    int bsnake, bp0, nb, bend;         // this block's B units: snake passes from bp0, or [jb0, jb1)
+    unsigned long long bsum[LW], target, lo, hi;
 };
+
+static_assert(sizeof(Misc) <= kLayerMiscBytes, "fused kernel block state outgrew its shared-memory region");
+
+// monotone unsigned key of a float (larger float -> larger key); -0 and +0
+// share the key of +0 so equal logits tie and the lower index wins
+__device__ __forceinline__ uint32_t fkey(float v) {
+    if (v == 0.f) v = 0.f;
+    const uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 
 // Snake over blocks: unit j -> block, pass by pass, reversing every other pass.
 __device__ __forceinline__ int snake_unit(int pass, int c, int G) {
@@ -319,7 +337,7 @@ struct LayerKernel {
                         const Act x = act_view(xq(tok[i]), a.H);
                         int is[FF::NSUB];
                         FF::isums(w, x, k0, nb, is);
-                        ag[i] += FF::combine(w, x, k0, nb, is);
+                        ag[i] = __fadd_rn(ag[i], FF::combine(w, x, k0, nb, is));
                     }
                 }
             }
@@ -333,7 +351,7 @@ struct LayerKernel {
                         const Act x = act_view(xq(tok[i]), a.H);
                         int is[FF::NSUB];
                         FF::isums(w, x, k0, nb, is);
-                        au[i] += FF::combine(w, x, k0, nb, is);
+                        au[i] = __fadd_rn(au[i], FF::combine(w, x, k0, nb, is));
                     }
                 }
             }
@@ -362,45 +380,106 @@ struct LayerKernel {
                 const int dest = U.kind == 0 ? i : plist()[uoff()[U.u] + i];
                 hb[(size_t)dest * Irows + row] = h;
             }
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) red_release(a.hctr + U.u, 1u);
+            if (lane == 0) m->hpend[U.u] += 1;
         }
         rbuf ^= 1;
     }
 
-    // requantise the h rows of unit U's expert into the block's hq records
-    __device__ bool load_hq(const Unit &U) {
-        const int key = U.kind == 2 ? MAXP : U.u;
-        if (m->hq_key == key) return true;
-        const int Irows = U.kind == 2 ? a.Is : a.I;
-        const unsigned need = (unsigned)(U.kind == 2 ? m->tilesIs : m->tilesI);
-        cbar();   // everyone is done with the previous hq
-        if (threadIdx.x == 0 && !m->abort)
-            if (!spin_geq(a.hctr + key, need)) fail();
-        cbar();
-        const float *hb = U.kind == 2 ? a.h_s : a.h_r;
-        const int chunks = (Irows + 255) / 256;
-        const bool ok = !m->abort;
-        for (int w = warp; ok && w < U.nt * chunks; w += LW) {
-            const int i = w / chunks, ch = w - i * chunks;
-            const int dest = U.kind == 2 ? i : plist()[uoff()[U.u] + i];
-            quant_chunk256<true>(hb + (size_t)dest * Irows, Irows, 256 * ch, hq(i), lane);
+    // make this block's h rows visible (one fence) and release the per-expert
+    // tickets it owes; called by warp 0 after a run of A units
+    __device__ void release_h(int nrouted) {
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence();
+            for (int u = -1; u < nrouted; ++u) {
+                const int key = u < 0 ? MAXP : u;
+                const int n = m->hpend[key];
+                if (n) { red_release(a.hctr + key, (unsigned)n); m->hpend[key] = 0; }
+            }
         }
-        if (threadIdx.x == 0) m->hq_key = key;
-        cbar();
-        return true;
+        __syncwarp();
     }
 
-    // B unit: o rows of the down projection, then (last block of the tile) y
+    // ---------------------------------------------------------- B phase
+    // The block's B units run in batches of consecutive units whose experts'
+    // requantised h fit the hq buffer together.  Per batch: wait for those
+    // experts' h tickets (one lane per expert), requantise every pair of them
+    // into hq (all warps), then unit b of the batch goes to warp b % 8, which
+    // streams its records in order and writes the o rows itself.
+
+    // expert key of B unit j: MAXP for the shared expert, else its unique index
+    __device__ int b_key(int j) {
+        if (j < m->nA + m->n_sb) return MAXP;
+        return (j - m->nA - m->n_sb) / m->tilesH;
+    }
+    __device__ int key_pairs(int key) { return key == MAXP ? a.T : uoff()[key + 1] - uoff()[key]; }
+
+    // From list entry n0, the longest run of B units whose distinct experts'
+    // pairs fit the hq buffer together (at most 64 experts, chosen by thread
+    // 0): wait for those experts' h tickets and requantise their h into hq.
+    // Returns the end of the run.
+    __device__ int load_hq_batch(int n0, int nend) {
+        int *kbase = m->kslot;
+        int *keys = m->kkey;
+        if (threadIdx.x == 0) {
+            int nk = 0, used = 0, n = n0;
+            for (; n < nend; ++n) {
+                const int key = b_key(b_unit(n));
+                bool seen = false;
+                for (int q = 0; q < nk; ++q) seen |= keys[q] == key;
+                if (seen) continue;
+                const int need = key_pairs(key);
+                if ((used + need > a.hq_slots || nk == 64) && n > n0) break;
+                keys[nk] = key;
+                kbase[nk] = used;
+                used += need;
+                ++nk;
+            }
+            m->nkeys = nk;
+            m->bend = n;
+        }
+        cbar();
+        const int nk = m->nkeys;
+        if (warp == 0 && !m->abort) {
+            for (int kk = lane; kk < nk; kk += 32) {
+                const int key = keys[kk];
+                const unsigned need = (unsigned)(key == MAXP ? m->tilesIs : m->tilesI);
+                if (!spin_geq(a.hctr + key, need)) fail();
+            }
+        }
+        cbar();
+        const bool ok = !m->abort;
+        // tasks: (key, pair, 256-chunk)
+        for (int kk = 0; ok && kk < nk; ++kk) {
+            const int key = keys[kk];
+            const int Irows = key == MAXP ? a.Is : a.I;
+            const float *hb = key == MAXP ? a.h_s : a.h_r;
+            const int chunks = (Irows + 255) / 256;
+            const int np = key_pairs(key);
+            for (int w = warp; w < np * chunks; w += LW) {
+                const int i = w / chunks, ch = w - i * chunks;
+                const int dest = key == MAXP ? i : plist()[uoff()[key] + i];
+                quant_chunk256<true>(hb + (size_t)dest * Irows, Irows, 256 * ch, hq(kbase[kk] + i), lane);
+            }
+        }
+        cbar();
+        return m->bend;
+    }
+
+    __device__ int key_slot(int key) {
+        for (int q = 0; q < m->nkeys; ++q)
+            if (m->kkey[q] == key) return m->kslot[q];
+        return 0;
+    }
+
+    // one B unit by one warp: records in order, then its o rows
     template <class FF>
-    __device__ void run_B(const Unit &U, int &item, int &rbuf) {
+    __device__ void run_B_warp(const Unit &U, int item, int slot0) {
         const int Irows = U.kind == 2 ? a.Is : a.I;
         float ao[NT];
 #pragma unroll
         for (int i = 0; i < NT; ++i) ao[i] = 0.f;
         for (int r = 0; r < U.nrec; ++r, ++item) {
-            if ((r & (LW - 1)) != warp) continue;
             const uint8_t *rec = wait_item(item);
             if (!rec) continue;
             typename FF::W wd;
@@ -411,54 +490,104 @@ struct LayerKernel {
 #pragma unroll
             for (int i = 0; i < NT; ++i) {
                 if (i < U.nt) {
-                    const Act h = act_view(hq(i), Irows);
+                    const Act h = act_view(hq(slot0 + i), Irows);
                     int is[FF::NSUB];
                     FF::isums(wd, h, k0, nb, is);
-                    ao[i] += FF::combine(wd, h, k0, nb, is);
+                    ao[i] = __fadd_rn(ao[i], FF::combine(wd, h, k0, nb, is));
                 }
             }
         }
-        float *red = reinterpret_cast<float *>(sm + o.red) + rbuf * (LW * 2 * NT * 32);
+        const int row = U.rt * 32 + lane;
+        const float bd = (U.kind == 3 && U.ex->b_down) ? U.ex->b_down[row] : 0.f;
 #pragma unroll
-        for (int i = 0; i < NT; ++i) red[(warp * NT + i) * 32 + lane] = ao[i];
-        cbar();
-        if (warp == 0) {
-            const int row = U.rt * 32 + lane;
-            for (int i = 0; i < U.nt && i < NT; ++i) {
-                float v = 0.f;
-#pragma unroll
-                for (int w = 0; w < LW; ++w) v += red[(w * NT + i) * 32 + lane];
+        for (int i = 0; i < NT; ++i) {
+            if (i < U.nt) {
                 if (U.kind == 3) {
-                    if (U.ex->b_down) v += U.ex->b_down[row];
                     const int p = plist()[uoff()[U.u] + i];
-                    a.o_r[(size_t)p * a.H + row] = v;
+                    a.o_r[(size_t)p * a.H + row] = U.ex->b_down ? ao[i] + bd : ao[i];
                 } else {
-                    a.o_s[(size_t)i * a.H + row] = v;
+                    a.o_s[(size_t)i * a.H + row] = ao[i];
                 }
             }
-            __threadfence();
-            __syncwarp();
-            unsigned old = 0;
-            if (lane == 0) old = atom_acqrel(a.yticket + U.rt, 1u);
-            old = __shfl_sync(0xFFFFFFFFu, old, 0);
-            if (old == (unsigned)m->nc - 1u) {
-                __syncwarp();
-                write_y(U.rt);
-                if (lane == 0) a.yticket[U.rt] = 0u;
-            }
         }
-        rbuf ^= 1;
+        if (lane == 0) atomicOr(&m->ytiles[U.rt >> 5], 1u << (U.rt & 31));
     }
 
-    // y rows of one 32-row tile: slots in slot order, shared expert last
+    __device__ void run_B_phase(int &item) {
+        const int nend = m->nb;
+        int n = 0;
+        while (n < nend) {
+            const int n1 = load_hq_batch(n, nend);
+            int it = item;
+            for (int q = n; q < n1; ++q) {
+                Unit U;
+                unit_of(b_unit(q), U);
+                if (((q - n) & (LW - 1)) == warp) {
+                    const int slot = key_slot(U.kind == 2 ? MAXP : U.u);
+                    if (U.kind == 2) run_B_warp<FS>(U, it, slot);
+                    else run_B_warp<F>(U, it, slot);
+                }
+                it += U.nrec;
+            }
+            item = it;
+            cbar();   // the next batch overwrites hq
+            n = n1;
+        }
+    }
+
+    // After this block's B units: every row tile it contributed to whose
+    // ticket shows all contributions writes its y rows.  The last contributor
+    // of a tile always sees the full count (its own release came last); any
+    // other block that also sees it writes the same values.
+    __device__ void finish_tiles() {
+        if (warp == 0) {   // one fence for all o rows, then this block's tile tickets
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence();
+                for (int w = 0; w < 8; ++w) {
+                    uint32_t bits = m->ytiles[w];
+                    while (bits) {
+                        red_release(a.yticket + 32 * w + __ffs(bits) - 1, 1u);
+                        bits &= bits - 1u;
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        cbar();
+        int n = 0;
+        for (int w = 0; w < 8; ++w) {
+            uint32_t bits = m->ytiles[w];
+            while (bits) {
+                const int rt = 32 * w + __ffs(bits) - 1;
+                bits &= bits - 1u;
+                if ((n++ % LW) != warp) continue;
+                unsigned v = 0;
+                if (lane == 0) v = ld_acquire(a.yticket + rt);
+                v = __shfl_sync(0xFFFFFFFFu, v, 0);
+                if (v >= (unsigned)m->nc) write_y(rt);
+            }
+        }
+    }
+
+    // y rows of one 32-row tile: slots in slot order, shared expert last.
+    // All loads of a token are issued before the sum (each is an L2 trip).
     __device__ void write_y(int rt) {
         const int row = rt * 32 + lane;
         for (int t = 0; t < a.T; ++t) {
             float y = 0.f;
-            for (int s = 0; s < a.k; ++s) {
-                const int p = t * a.k + s;
-                if (pu()[p] < 0) continue;
-                y += wts()[p] * __ldcg(a.o_r + (size_t)p * a.H + row);
+            for (int s0 = 0; s0 < a.k; s0 += 8) {
+                float v[8];
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int s = s0 + jj, p = t * a.k + s;
+                    v[jj] = (s < a.k && pu()[p] >= 0) ? __ldcg(a.o_r + (size_t)p * a.H + row) : 0.f;
+                }
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int s = s0 + jj, p = t * a.k + s;
+                    if (s < a.k && pu()[p] >= 0) y += wts()[p] * v[jj];
+                }
             }
             if (a.shared) y += __ldcg(a.o_s + (size_t)t * a.H + row);
             a.y[(size_t)t * a.H + row] = y;
@@ -472,8 +601,8 @@ struct LayerKernel {
             mbar_init(fixed_bar(), 1);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             m->abort = 0;
-            m->hq_key = -1;
         }
+        for (int i = threadIdx.x; i <= MAXP; i += LT) m->hpend[i] = 0;
         __syncthreads();
     }
 
@@ -579,9 +708,44 @@ struct LayerKernel {
             if (a.rbias) l = __fadd_rn(l, a.rbias[e0 + r]);
             a.logits[(size_t)t * a.E + e0 + r] = l;
         }
-        __threadfence();
         cbar();
-        if (threadIdx.x == 0) red_release(a.route_ctr, 1u);
+        if (threadIdx.x == 0) {
+            __threadfence();
+            red_release(a.route_ctr, 1u);
+        }
+    }
+
+    // k largest of E logits (largest first, lower index on equal logits) by one
+    // warp: lane l holds keys of experts l + 32 j in registers; each round takes
+    // the warp maximum key, then the lowest index holding it.  Returns, in lane
+    // s < k, the s-th selected logit.
+    template <int JN>
+    __device__ float select_topk(const float *lg, int *out) {
+        uint32_t key[JN];
+#pragma unroll
+        for (int j = 0; j < JN; ++j) {
+            const int e = lane + 32 * j;
+            key[j] = e < a.E ? fkey(lg[e]) : 0u;
+        }
+        float mysel = 0.f;
+        for (int s = 0; s < a.k; ++s) {
+            uint32_t best = 0u;
+            int bj = 0;
+#pragma unroll
+            for (int j = 0; j < JN; ++j)
+                if (key[j] > best) { best = key[j]; bj = j; }
+            const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, best);
+            const int cand = (best == mx && best != 0u) ? lane + 32 * bj : 0x7FFFFFFF;
+            const int win = __reduce_min_sync(0xFFFFFFFFu, cand);
+            if ((win & 31) == lane) {
+#pragma unroll
+                for (int j = 0; j < JN; ++j)
+                    if (j == (win >> 5)) key[j] = 0u;
+            }
+            if (lane == s) mysel = fkey_value(mx);
+            if (lane == 0) out[s] = win;
+        }
+        return mysel;
     }
 
     __device__ void topk_and_group() {
@@ -591,30 +755,21 @@ struct LayerKernel {
         float *lgs = reinterpret_cast<float *>(sm + o.lg);
         for (int i = threadIdx.x; i < a.T * a.E; i += LW * 32) lgs[i] = __ldcg(a.logits + i);
         cbar();
-        if (c == 0 && a.logits_out)
-            for (int i = threadIdx.x; i < a.T * a.E; i += LW * 32) a.logits_out[i] = lgs[i];
         for (int t = warp; t < a.T; t += LW) {
             const float *lg = lgs + (size_t)t * a.E;
-            uint32_t taken = 0;
-            float mysel = 0.f;
-            for (int s = 0; s < a.k; ++s) {
-                float bv = 0.f;
-                int bi = 0x7FFFFFFF;
-                for (int j = 0, e = lane; e < a.E; ++j, e += 32) {
-                    if (taken & (1u << j)) continue;
-                    const float v = lg[e];
-                    if (bi == 0x7FFFFFFF || v > bv) { bv = v; bi = e; }
-                }
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) {
-                    const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-                    const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-                    if (oi != 0x7FFFFFFF && (bi == 0x7FFFFFFF || ov > bv || (ov == bv && oi < bi))) { bv = ov; bi = oi; }
-                }
-                if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-                if (lane == s) mysel = bv;
-                if (lane == 0) ids()[t * a.k + s] = bi;
-            }
+            const float mysel = a.E <= 256 ? select_topk<8>(lg, ids() + t * a.k) : select_topk<32>(lg, ids() + t * a.k);
+            if (lane < a.k) wts()[t * a.k + lane] = mysel;   // the weights replace these later
+        }
+        cbar();
+        group();
+    }
+
+    // gating weights from the selected logits (after the expert streams started)
+    __device__ void gating_weights() {
+        const float *lgs = reinterpret_cast<const float *>(sm + o.lg);
+        for (int t = warp; t < a.T; t += LW) {
+            const float *lg = lgs + (size_t)t * a.E;
+            const float mysel = lane < a.k ? wts()[t * a.k + lane] : 0.f;
             const float l0 = __shfl_sync(0xFFFFFFFFu, mysel, 0);
             float w;
             if (a.gating == MOE_GATE_SOFTMAX) {
@@ -642,88 +797,138 @@ struct LayerKernel {
         }
         cbar();
         if (c == 0) {
+            if (a.logits_out)
+                for (int i = threadIdx.x; i < a.T * a.E; i += LW * 32) a.logits_out[i] = lgs[i];
             for (int i = threadIdx.x; i < a.P; i += LW * 32) {
                 if (a.ids_out) a.ids_out[i] = ids()[i];
                 if (a.w_out) a.w_out[i] = wts()[i];
             }
         }
-        group();
     }
 
-    // (token, slot) pairs grouped by owned expert, ascending ids, tokens ascending
+    // (token, slot) pairs grouped by owned expert, ascending ids, tokens
+    // ascending; built by warp 0 alone (warp-synchronous, no block barriers)
     __device__ void group() {
-        const int tid = threadIdx.x, P = a.P;
-        const int nw = (a.E + 31) >> 5;
-        for (int i = tid; i < MOE_MAX_EXPERTS / 32; i += LW * 32) m->bitmap[i] = 0;
-        for (int i = tid; i < P; i += LW * 32) umask()[i] = 0;
-        cbar();
-        const moe_expert *T = table();
-        for (int p = tid; p < P; p += LW * 32) {
-            const int t = p / a.k, s = p - t * a.k;
-            const int e = ids()[p];
-            bool dup = false;
-            for (int s2 = 0; s2 < s; ++s2) dup |= (ids()[t * a.k + s2] == e);
-            const bool keep = !dup && T[e].gate != nullptr;
-            pu()[p] = keep ? e : -1;
-            if (keep) atomicOr(&m->bitmap[e >> 5], 1u << (e & 31));
-        }
-        cbar();
-        if (tid < 32) {
+        if (a.T == 1 && warp == 0) {
+            // one token: the k ids are distinct, each expert has one pair; the
+            // unique list is the owned ids in ascending order
+            const moe_expert *T = table();
+            const int e = lane < a.k ? ids()[lane] : 0x7FFFFFFF;
+            const bool own = lane < a.k && T[e].gate != nullptr;
+            const unsigned ownm = __ballot_sync(0xFFFFFFFFu, own);
+            int rank = 0;
+            for (int j = 0; j < a.k; ++j) {
+                const int ej = __shfl_sync(0xFFFFFFFFu, e, j);
+                rank += ((ownm >> j) & 1u) && ej < e;
+            }
+            const int U = __popc(ownm);
+            if (lane < a.k) pu()[lane] = own ? rank : -1;
+            if (own) {
+                ue()[rank] = e;
+                umask()[rank] = 1u;
+                uoff()[rank] = rank;
+                plist()[rank] = lane;
+            }
+            if (lane == 0) { uoff()[U] = U; m->U = U; }
+        } else if (warp == 0) {
+            const int nw = (a.E + 31) >> 5;
+            m->bitmap[lane] = 0u;   // MOE_MAX_EXPERTS / 32 == 32 words
+            __syncwarp();
+            const moe_expert *T = table();
+            // the selection gives k distinct ids per token: only ownership filters
+            for (int t = 0; t < a.T; ++t)
+                for (int s = lane; s < a.k; s += 32) {
+                    const int p = t * a.k + s;
+                    const int e = ids()[p];
+                    const bool keep = T[e].gate != nullptr;
+                    pu()[p] = keep ? e : -1;
+                    if (keep) atomicOr(&m->bitmap[e >> 5], 1u << (e & 31));
+                }
+            __syncwarp();
+            const int cnt = lane < nw ? __popc(m->bitmap[lane]) : 0;
+            int inc = cnt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xFFFFFFFFu, inc, off);
+                if (lane >= off) inc += v;
+            }
+            m->wpre[lane] = inc - cnt;
+            const int U = __shfl_sync(0xFFFFFFFFu, inc, 31);
+            for (int u = lane; u < U; u += 32) umask()[u] = 0u;
+            __syncwarp();
+            for (int t = 0; t < a.T; ++t)
+                for (int s = lane; s < a.k; s += 32) {
+                    const int p = t * a.k + s;
+                    const int e = pu()[p];
+                    if (e < 0) continue;
+                    const int u = m->wpre[e >> 5] + __popc(m->bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
+                    ue()[u] = e;
+                    atomicOr(&umask()[u], 1u << t);
+                    pu()[p] = u;
+                }
+            __syncwarp();
             int carry = 0;
-            for (int base = 0; base < nw; base += 32) {
-                const int w = base + tid;
-                const int cnt = w < nw ? __popc(m->bitmap[w]) : 0;
-                int inc = cnt;
+            for (int base = 0; base < U; base += 32) {
+                const int u = base + lane;
+                const int c2 = u < U ? __popc(umask()[u]) : 0;
+                int in2 = c2;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
-                    const int v = __shfl_up_sync(0xFFFFFFFFu, inc, off);
-                    if (tid >= off) inc += v;
+                    const int v = __shfl_up_sync(0xFFFFFFFFu, in2, off);
+                    if (lane >= off) in2 += v;
                 }
-                if (w < nw) m->wpre[w] = carry + inc - cnt;
-                carry += __shfl_sync(0xFFFFFFFFu, inc, 31);
+                if (u < U) uoff()[u] = carry + in2 - c2;
+                carry += __shfl_sync(0xFFFFFFFFu, in2, 31);
             }
-            if (tid == 0) m->U = carry;
-        }
-        cbar();
-        for (int p = tid; p < P; p += LW * 32) {
-            const int e = pu()[p];
-            if (e < 0) continue;
-            const int u = m->wpre[e >> 5] + __popc(m->bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
-            ue()[u] = e;
-            atomicOr(&umask()[u], 1u << (p / a.k));
-            pu()[p] = u;
-        }
-        cbar();
-        if (tid < 32) {
-            int carry = 0;
-            for (int base = 0; base < m->U; base += 32) {
-                const int u = base + tid;
-                const int cnt = u < m->U ? __popc(umask()[u]) : 0;
-                int inc = cnt;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const int v = __shfl_up_sync(0xFFFFFFFFu, inc, off);
-                    if (tid >= off) inc += v;
+            if (lane == 0) { uoff()[U] = carry; m->U = U; }
+            __syncwarp();
+            for (int t = 0; t < a.T; ++t)
+                for (int s = lane; s < a.k; s += 32) {
+                    const int p = t * a.k + s;
+                    const int u = pu()[p];
+                    if (u < 0) continue;
+                    plist()[uoff()[u] + __popc(umask()[u] & ((1u << t) - 1u))] = p;
                 }
-                if (u < m->U) uoff()[u] = carry + inc - cnt;
-                carry += __shfl_sync(0xFFFFFFFFu, inc, 31);
-            }
-            if (tid == 0) uoff()[m->U] = carry;
-        }
-        cbar();
-        for (int p = tid; p < P; p += LW * 32) {
-            const int u = pu()[p];
-            if (u < 0) continue;
-            const int t = p / a.k;
-            plist()[uoff()[u] + __popc(umask()[u] & ((1u << t) - 1u))] = p;
         }
         cbar();
         plan();
     }
 
-    // unit counts and this block's B range (bytes balanced against the A deal)
+    // unit counts and this block's B range: every block's A bytes follow from
+    // the snake deal; block c gets the B units whose byte midpoints fall in
+    // its share of what is left to reach the mean (integer bytes throughout,
+    // so every block computes the same boundaries)
     __device__ void plan() {
+        typedef unsigned long long u64;
         const int tid = threadIdx.x;
+        if (a.T == 1) {
+            // one snake over A units then B units: B units of a block belong to
+            // different experts, but every expert has a single pair, so one hq
+            // batch holds them all
+            if (tid == 0) {
+                m->tilesI = a.I / 32;
+                m->tilesIs = a.shared ? a.Is / 32 : 0;
+                m->tilesH = a.H / 32;
+                m->n_ra = m->U * m->tilesI;
+                m->nA = m->n_sa + m->n_ra;
+                m->n_sb = a.shared ? m->tilesH : 0;
+                m->n_rb = m->U * m->tilesH;
+                m->nB = m->n_sb + m->n_rb;
+                m->nc = m->U + (a.shared ? 1 : 0);
+                m->bsnake = 1;
+                int p = 0;
+                while (snake_unit(p, c, G) < m->nA) ++p;
+                m->bp0 = p;
+                int n = 0;
+                while (snake_unit(p + n, c, G) < m->nA + m->nB) ++n;
+                m->nb = n;
+            }
+            if (tid < 8) m->ytiles[tid] = 0u;
+            cbar();
+            return;
+        }
+        const u64 sa = 2ull * FS::tile_bytes(a.H), ra = 2ull * F::tile_bytes(a.H);
+        const u64 sb = a.shared ? (u64)FS::tile_bytes(a.Is) : 0ull, rb = (u64)F::tile_bytes(a.I);
         if (tid == 0) {
             m->tilesI = a.I / 32;
             m->tilesIs = a.shared ? a.Is / 32 : 0;
@@ -734,66 +939,66 @@ struct LayerKernel {
             m->n_rb = m->U * m->tilesH;
             m->nB = m->n_sb + m->n_rb;
             m->nc = m->U + (a.shared ? 1 : 0);
+            const u64 tot = (u64)m->n_sa * sa + (u64)m->n_ra * ra + (u64)m->n_sb * sb + (u64)m->n_rb * rb;
+            m->target = (u64)((float)tot / (float)G) + 1ull;   // any fixed rule works: all blocks agree
         }
+        if (tid < 8) m->ytiles[tid] = 0u;
         cbar();
-        const double sa = 2.0 * FS::tile_bytes(a.H), ra = 2.0 * F::tile_bytes(a.H);
-        const double sb = a.shared ? (double)FS::tile_bytes(a.Is) : 0.0, rb = (double)F::tile_bytes(a.I);
-        const double totB = m->n_sb * sb + m->n_rb * rb;
-        double totA = m->n_sa * sa + m->n_ra * ra;
-        // A bytes of block tid (tid < G), then budgets, scan
-        double my_a = 0.0;
+        u64 my_a = 0;
         if (tid < G) {
-            for (int p = 0;; ++p) {
+            for (int p = 0; p * G < m->nA; ++p) {
                 const int j = snake_unit(p, tid, G);
-                if (p * G >= m->nA) break;
                 if (j < m->n_sa) my_a += sa;
                 else if (j < m->nA) my_a += ra;
             }
         }
-        const double target = (totA + totB) / G;
-        double b = (tid < G) ? fmax(0.0, target - my_a) : 0.0;
-        // block-exclusive scan of b over the first G threads (8 warps x 32)
-        double inc = b;
+        const u64 b = (tid < G && m->target > my_a) ? m->target - my_a : 0ull;
+        u64 inc = b;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const double v = __shfl_up_sync(0xFFFFFFFFu, inc, off);
+            const u64 v = __shfl_up_sync(0xFFFFFFFFu, inc, off);
             if (lane >= off) inc += v;
         }
         if (lane == 31) m->bsum[warp] = inc;
         cbar();
-        double before = 0.0, total = 0.0;
-        for (int w = 0; w < LW; ++w) {
-            if (w < warp) before += m->bsum[w];
-            total += m->bsum[w];
-        }
-        const double excl = before + inc - b;
-        // block c's range [P_c, P_{c+1}) scaled to totB
-        __shared__ double s_lo, s_hi;
-        const double scale = total > 0.0 ? totB / total : 0.0;
-        if (tid == c) s_lo = excl * scale;
-        if (tid == c + 1 || (c + 1 == G && tid == 0)) s_hi = (c + 1 == G) ? totB : excl * scale;
+        u64 before = 0;
+        for (int w = 0; w < warp; ++w) before += m->bsum[w];
+        const u64 excl = before + inc - b;
+        if (tid == c) m->lo = excl;
+        if (tid == c + 1) m->hi = excl;
         cbar();
         if (tid == 0) {
-            m->jb0 = first_b_unit(s_lo, sb, rb);
-            m->jb1 = (c + 1 == G) ? m->nB : first_b_unit(s_hi, sb, rb);
+            m->jb0 = first_b_unit(m->lo, sb, rb);
+            m->jb1 = (c + 1 == G) ? m->nB : first_b_unit(m->hi, sb, rb);
             if (m->jb1 < m->jb0) m->jb1 = m->jb0;
+            m->bsnake = 0;
+            m->nb = m->jb1 - m->jb0;
         }
         cbar();
     }
 
-    // first B unit whose byte midpoint is >= X
-    __device__ int first_b_unit(double X, double sb, double rb) {
-        const int n_sb = m->n_sb, n_rb = m->n_rb;
-        if (n_sb > 0) {
-            double jj = ceil((X - 0.5 * sb) / sb);
-            if (jj < 0) jj = 0;
-            if (jj < n_sb) return (int)jj;
-        }
-        const double base = n_sb * sb;
-        double jj = ceil((X - base - 0.5 * rb) / rb);
-        if (jj < 0) jj = 0;
-        if (jj > n_rb) jj = n_rb;
-        return n_sb + (int)jj;
+    // the n-th B unit of this block (global unit index)
+    __device__ int b_unit(int n) {
+        return m->bsnake ? snake_unit(m->bp0 + n, c, G) : m->nA + m->jb0 + n;
+    }
+
+    // first B unit whose byte midpoint is >= X (B list: shared units of sb
+    // bytes, then routed units of rb bytes)
+    __device__ int first_b_unit(unsigned long long X, unsigned long long sb, unsigned long long rb) {
+        typedef unsigned long long u64;
+        const int n_sb = m->n_sb, nB = m->nB;
+        auto mid = [&](int j) -> u64 {
+            return j < n_sb ? (u64)j * sb + sb / 2 : (u64)n_sb * sb + (u64)(j - n_sb) * rb + rb / 2;
+        };
+        // fp32 estimate, then exact integer correction
+        int j;
+        if (n_sb > 0 && X <= mid(n_sb - 1)) j = (int)((float)X / (float)sb);
+        else j = n_sb + (int)((float)(X > (u64)n_sb * sb ? X - (u64)n_sb * sb : 0ull) / (float)rb);
+        if (j > nB) j = nB;
+        if (j < 0) j = 0;
+        while (j < nB && mid(j) < X) ++j;
+        while (j > 0 && mid(j - 1) >= X) --j;
+        return j;
     }
 
     // ------------------------------------------------------- main body
@@ -841,8 +1046,8 @@ struct LayerKernel {
                 if (p * G >= m->nA) break;
                 if (j >= m->n_sa && j < m->nA && !issue_unit(R, j)) break;
             }
-            for (int j = m->nA + m->jb0; j < m->nA + m->jb1 && !m->abort; ++j)
-                if (!issue_unit(R, j)) break;
+            for (int n = 0; n < m->nb && !m->abort; ++n)
+                if (!issue_unit(R, b_unit(n))) break;
         }
         // drain: no copy may still be writing this block's shared memory at exit
         if (lane == 0) {
@@ -872,8 +1077,10 @@ struct LayerKernel {
                 run_A<FS>(U, item, rbuf);
             }
         }
+        if (warp == 0) release_h(0);
         topk_and_group();
         bar_handoff();
+        gating_weights();
         for (int p = 0;; ++p) {
             const int j = snake_unit(p, c, G);
             if (p * G >= m->nA) break;
@@ -883,15 +1090,11 @@ struct LayerKernel {
                 run_A<F>(U, item, rbuf);
             }
         }
+        if (warp == 0) release_h(m->U);
         // no loop below leaves early: every consumer thread must reach every
         // named barrier; after a timeout only waits and sums are skipped
-        for (int j = m->nA + m->jb0; j < m->nA + m->jb1; ++j) {
-            Unit U;
-            unit_of(j, U);
-            load_hq(U);
-            if (U.kind == 2) run_B<FS>(U, item, rbuf);
-            else run_B<F>(U, item, rbuf);
-        }
+        run_B_phase(item);
+        finish_tiles();
         if (m->nB == 0 && c == 0) {   // nothing owned: y = 0
             for (int i = threadIdx.x; i < a.T * a.H; i += LW * 32) a.y[i] = 0.f;
         }

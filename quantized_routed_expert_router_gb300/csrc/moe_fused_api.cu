@@ -12,7 +12,7 @@ cudaError_t launch_layer_mx4(const LayerArgs &a, int sqtype, int G, size_t smem,
 
 // constants mirrored from moe_fused.cuh (kept in one place there; checked below)
 constexpr int kLW = 8, kNBAR = 32;
-constexpr uint32_t kRingDefault = 80 * 1024;
+constexpr uint32_t kRingDefault = 160 * 1024;
 
 static size_t al16(size_t v) { return (v + 15) & ~(size_t)15; }
 
@@ -67,6 +67,12 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
     const int Imax = a.Is > a.I ? a.Is : a.I;
     a.hrec = q8_row_bytes(Imax);
     a.NT = a.T <= 1 ? 1 : (a.T <= 4 ? 4 : 16);
+    {   // enough hq records for every pair when they fit in 48 KB, at least one expert's (T)
+        const size_t want = (size_t)a.P + (a.shared ? a.T : 0);
+        size_t fit = (48 * 1024) / a.hrec;
+        if (fit < (size_t)a.T) fit = a.T;
+        a.hq_slots = (int)(want < fit ? want : fit);
+    }
 
     Smem o;
     size_t off = 0;
@@ -77,9 +83,9 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
     };
     const size_t fixed_router = (size_t)rr * rowb;
     const size_t fixed_rest = (2 * kNBAR + 1) * 8 + kNBAR * 4 + fixed_router +
-                              (a.table_in_smem ? a.E * sizeof(moe_expert) : 0) + a.T * a.xrec + a.T * a.hrec +
+                              (a.table_in_smem ? a.E * sizeof(moe_expert) : 0) + a.T * a.xrec + (size_t)a.hq_slots * a.hrec +
                               4 * (size_t)a.T * a.E + 4 * (size_t)rr * nseg * a.T + 8 * (size_t)a.P +
-                              4 * (5 * (size_t)a.P + 1) + 2 * kLW * 2 * a.NT * 32 * 4 + 2048 + 16 * 16;
+                              4 * (5 * (size_t)a.P + 1) + 2 * kLW * 2 * a.NT * 32 * 4 + kLayerMiscBytes + 16 * 16;
     const size_t optin = (size_t)smem_optin();
     if (fixed_rest + 2 * (size_t)item > optin) return cudaErrorInvalidConfiguration;
     size_t ring = kRingDefault;
@@ -92,14 +98,14 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
     o.router = take(fixed_router);
     o.table = take(a.table_in_smem ? a.E * sizeof(moe_expert) : 0);
     o.xq = take(a.T * a.xrec);
-    o.hq = take(a.T * a.hrec);
+    o.hq = take((size_t)a.hq_slots * a.hrec);
     o.lg = take(4 * (size_t)a.T * a.E);
     o.segv = take(4 * (size_t)rr * nseg * a.T);
     o.ids = take(4 * (size_t)a.P);
     o.wts = take(4 * (size_t)a.P);
     o.grp = take(4 * (5 * (size_t)a.P + 1));
     o.red = take(2 * kLW * 2 * a.NT * 32 * 4);
-    o.misc = take(2048);
+    o.misc = take(kLayerMiscBytes);
     o.total = (uint32_t)off;
     if (o.total > optin) return cudaErrorInvalidConfiguration;
     a.sm = o;

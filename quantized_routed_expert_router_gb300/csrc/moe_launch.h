@@ -11,6 +11,7 @@
 namespace moe {
 
 constexpr int MAXP = MOE_MAX_TOKENS * MOE_MAX_K;   // (token, slot) pairs per call
+constexpr size_t kLayerMiscBytes = 4096;          // shared-memory block state of the fused kernel
 
 struct RouteArgs {
     const float *hidden;
@@ -63,6 +64,7 @@ struct LayerArgs {
     int rtype, k, gating, renorm;
     int T, H, I, Is, E, P, NT;
     int table_in_smem;
+    int hq_slots;                   // q8 records of requantised h the block can hold
     uint32_t ring_bytes;
     size_t xrec, hrec;
     Smem sm;
