@@ -163,6 +163,11 @@ struct LayerKernel {
     __device__ uint64_t *empty_bar(int i) { return reinterpret_cast<uint64_t *>(sm + o.bars) + NBAR + (i % NBAR); }
     __device__ uint64_t *fixed_bar() { return reinterpret_cast<uint64_t *>(sm + o.bars) + 2 * NBAR; }
     __device__ uint32_t *starts() { return reinterpret_cast<uint32_t *>(sm + o.starts); }
+    // item index currently owning each ring slot (set by the producer once the
+    // slot's previous item is reclaimed); lets a consumer that is many items
+    // ahead of the ring wait for its own item instead of an earlier phase of
+    // the same barrier with the same parity
+    __device__ volatile uint32_t *tags() { return reinterpret_cast<volatile uint32_t *>(sm + o.starts) + NBAR; }
     __device__ const moe_expert *table() {
         return a.table_in_smem ? reinterpret_cast<const moe_expert *>(sm + o.table) : a.experts;
     }
@@ -272,6 +277,7 @@ struct LayerKernel {
         if (!ring_place(R, bytes, start)) return false;
         const int i = R.issued;
         starts()[i % NBAR] = start;
+        tags()[i % NBAR] = (uint32_t)i;
         uint8_t *dst = sm + o.ring + start;
         uint64_t *fb = full_bar(i);
         mbar_arm(fb, bytes);
@@ -304,6 +310,11 @@ struct LayerKernel {
     // wait for item i (a record, or a gate+up record pair) to land in the ring
     __device__ const uint8_t *wait_item(int i) {
         if (m->abort) return nullptr;
+        if (tags()[i % NBAR] != (uint32_t)i) {
+            const long long t0 = clock64();
+            while (tags()[i % NBAR] != (uint32_t)i)
+                if (clock64() - t0 > WAIT_CYCLES || m->abort) { fail(); return nullptr; }
+        }
         if (!mbar_wait(full_bar(i), (uint32_t)((i / NBAR) & 1))) { fail(); return nullptr; }
         return sm + o.ring + starts()[i % NBAR];
     }
@@ -356,7 +367,10 @@ struct LayerKernel {
                 }
             }
         }
-        float *red = reinterpret_cast<float *>(sm + o.red) + rbuf * (LW * 2 * NT * 32);
+        // NT <= 4: two reduction buffers alternate; NT = 16: one buffer, and
+        // the barrier below keeps it until warp 0 has read the previous unit
+        if (NT > 4) cbar();
+        float *red = reinterpret_cast<float *>(sm + o.red) + (NT <= 4 ? rbuf : 0) * (LW * 2 * NT * 32);
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
             red[((warp * 2 + 0) * NT + i) * 32 + lane] = ag[i];
@@ -603,6 +617,7 @@ struct LayerKernel {
             m->abort = 0;
         }
         for (int i = threadIdx.x; i <= MAXP; i += LT) m->hpend[i] = 0;
+        for (int i = threadIdx.x; i < NBAR; i += LT) tags()[i] = 0xFFFFFFFFu;
         __syncthreads();
     }
 

@@ -67,12 +67,7 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
     const int Imax = a.Is > a.I ? a.Is : a.I;
     a.hrec = q8_row_bytes(Imax);
     a.NT = a.T <= 1 ? 1 : (a.T <= 4 ? 4 : 16);
-    {   // enough hq records for every pair when they fit in 48 KB, at least one expert's (T)
-        const size_t want = (size_t)a.P + (a.shared ? a.T : 0);
-        size_t fit = (48 * 1024) / a.hrec;
-        if (fit < (size_t)a.T) fit = a.T;
-        a.hq_slots = (int)(want < fit ? want : fit);
-    }
+    const size_t red_bytes = (size_t)(a.NT <= 4 ? 2 : 1) * kLW * 2 * a.NT * 32 * 4;
 
     Smem o;
     size_t off = 0;
@@ -82,11 +77,24 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
         return (uint32_t)at;
     };
     const size_t fixed_router = (size_t)rr * rowb;
-    const size_t fixed_rest = (2 * kNBAR + 1) * 8 + kNBAR * 4 + fixed_router +
-                              (a.table_in_smem ? a.E * sizeof(moe_expert) : 0) + a.T * a.xrec + (size_t)a.hq_slots * a.hrec +
+    // everything but the ring and the hq records
+    const size_t fixed_core = (2 * kNBAR + 1) * 8 + 2 * kNBAR * 4 + fixed_router +
+                              (a.table_in_smem ? a.E * sizeof(moe_expert) : 0) + a.T * a.xrec +
                               4 * (size_t)a.T * a.E + 4 * (size_t)rr * nseg * a.T + 8 * (size_t)a.P +
-                              4 * (5 * (size_t)a.P + 1) + 2 * kLW * 2 * a.NT * 32 * 4 + kLayerMiscBytes + 16 * 16;
+                              4 * (5 * (size_t)a.P + 1) + red_bytes + kLayerMiscBytes + 16 * 16;
     const size_t optin = (size_t)smem_optin();
+    {   // hq records: every pair when they fit in 48 KB and leave room for the
+        // ring, never fewer than one expert's (T)
+        const size_t want = (size_t)a.P + (a.shared ? a.T : 0);
+        size_t fit = (48 * 1024) / a.hrec;
+        if (fixed_core + 2 * (size_t)item < optin) {
+            const size_t room = (optin - fixed_core - 2 * (size_t)item) / a.hrec;
+            if (room < fit) fit = room;
+        }
+        if (fit < (size_t)a.T) fit = a.T;
+        a.hq_slots = (int)(want < fit ? want : fit);
+    }
+    const size_t fixed_rest = fixed_core + (size_t)a.hq_slots * a.hrec;
     if (fixed_rest + 2 * (size_t)item > optin) return cudaErrorInvalidConfiguration;
     size_t ring = kRingDefault;
     if (ring < 2 * (size_t)item) ring = 2 * (size_t)item;
@@ -94,7 +102,7 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
     a.ring_bytes = (uint32_t)ring;
     o.ring = take(ring);
     o.bars = take((2 * kNBAR + 1) * 8);
-    o.starts = take(kNBAR * 4);
+    o.starts = take(2 * kNBAR * 4);   // item start offsets, then slot tags
     o.router = take(fixed_router);
     o.table = take(a.table_in_smem ? a.E * sizeof(moe_expert) : 0);
     o.xq = take(a.T * a.xrec);
@@ -104,7 +112,7 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
     o.ids = take(4 * (size_t)a.P);
     o.wts = take(4 * (size_t)a.P);
     o.grp = take(4 * (5 * (size_t)a.P + 1));
-    o.red = take(2 * kLW * 2 * a.NT * 32 * 4);
+    o.red = take(red_bytes);
     o.misc = take(kLayerMiscBytes);
     o.total = (uint32_t)off;
     if (o.total > optin) return cudaErrorInvalidConfiguration;
