@@ -391,17 +391,12 @@ struct FMX4 {
 // the width is not a multiple of 256): amax = max|x|, d = amax/127,
 // q = rint(x * (127/amax)) with IEEE division and round-half-to-even, d = 0
 // and q = 0 for an all-zero block, and the sums of each 16 codes.
-//
-// One warp quantises 256 consecutive elements (lane l: elements 8l..8l+7) of
-// one row and writes them into the row's q8 record.  `coherent` selects L2
-// loads for data another block of the same grid has just written.
+
+// lane l's 8 elements (8l..8l+7 of the 256-chunk at c0); false past the row
 template <bool coherent>
-__device__ __forceinline__ void quant_chunk256(const float *x, int n, int c0, uint8_t *rec, int lane) {
-    const int B = act_block(n);
+__device__ __forceinline__ bool quant_load8(const float *x, int n, int c0, int lane, float v[8]) {
     const int e0 = c0 + 8 * lane;
-    const bool active = e0 < n;
-    float v[8];
-    if (active) {
+    if (e0 < n) {
         float4 a, b;
         if (coherent) {
             a = __ldcg(reinterpret_cast<const float4 *>(x + e0));
@@ -412,10 +407,17 @@ __device__ __forceinline__ void quant_chunk256(const float *x, int n, int c0, ui
         }
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        return true;
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    return false;
+}
+
+// quantise a warp's 256-chunk (values already loaded) into the q8 record
+__device__ __forceinline__ void quant_store8(const float v[8], bool active, int n, int c0, uint8_t *rec, int lane) {
+    const int B = act_block(n);
+    const int e0 = c0 + 8 * lane;
     uint32_t am = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) am = max(am, __float_as_uint(fabsf(v[i])));
@@ -454,6 +456,16 @@ __device__ __forceinline__ void quant_chunk256(const float *x, int n, int c0, ui
             reinterpret_cast<float *>(rec)[e0 >> 5] = d;
         }
     }
+}
+
+// One warp quantises 256 consecutive elements (lane l: elements 8l..8l+7) of
+// one row and writes them into the row's q8 record.  `coherent` selects L2
+// loads for data another block of the same grid has just written.
+template <bool coherent>
+__device__ __forceinline__ void quant_chunk256(const float *x, int n, int c0, uint8_t *rec, int lane) {
+    float v[8];
+    const bool active = quant_load8<coherent>(x, n, c0, lane, v);
+    quant_store8(v, active, n, c0, rec, lane);
 }
 
 }  // namespace moe

@@ -399,12 +399,11 @@ struct LayerKernel {
         rbuf ^= 1;
     }
 
-    // make this block's h rows visible (one fence) and release the per-expert
-    // tickets it owes; called by warp 0 after a run of A units
+    // release the per-expert h tickets this block owes (its h rows were all
+    // written by warp 0); called by warp 0 after a run of A units
     __device__ void release_h(int nrouted) {
-        __syncwarp();
+        __syncwarp();   // orders every lane's h stores before lane 0's releases
         if (lane == 0) {
-            __threadfence();
             for (int u = -1; u < nrouted; ++u) {
                 const int key = u < 0 ? MAXP : u;
                 const int n = m->hpend[key];
@@ -463,18 +462,46 @@ struct LayerKernel {
         }
         cbar();
         const bool ok = !m->abort;
-        // tasks: (key, pair, 256-chunk)
-        for (int kk = 0; ok && kk < nk; ++kk) {
+        // tasks (key, pair, 256-chunk), flattened; a warp loads the h of up to
+        // four tasks before quantising them (each load is an L2 trip)
+        int ntask = 0;
+        for (int kk = 0; kk < nk; ++kk) {
             const int key = keys[kk];
             const int Irows = key == MAXP ? a.Is : a.I;
-            const float *hb = key == MAXP ? a.h_s : a.h_r;
-            const int chunks = (Irows + 255) / 256;
-            const int np = key_pairs(key);
-            for (int w = warp; w < np * chunks; w += LW) {
-                const int i = w / chunks, ch = w - i * chunks;
+            ntask += key_pairs(key) * ((Irows + 255) / 256);
+        }
+        for (int w0 = warp; ok && w0 < ntask; w0 += 4 * LW) {
+            float v[4][8];
+            bool act[4];
+            const float *src[4];
+            uint8_t *dst[4];
+            int cidx[4], nrow[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int w = w0 + q * LW;
+                act[q] = false;
+                if (w >= ntask) continue;
+                int rem = w, kk = 0;
+                for (;; ++kk) {   // locate the task's expert
+                    const int Ir = keys[kk] == MAXP ? a.Is : a.I;
+                    const int nt = key_pairs(keys[kk]) * ((Ir + 255) / 256);
+                    if (rem < nt) break;
+                    rem -= nt;
+                }
+                const int key = keys[kk];
+                const int Irows = key == MAXP ? a.Is : a.I;
+                const int chunks = (Irows + 255) / 256;
+                const int i = rem / chunks, ch = rem - i * chunks;
                 const int dest = key == MAXP ? i : plist()[uoff()[key] + i];
-                quant_chunk256<true>(hb + (size_t)dest * Irows, Irows, 256 * ch, hq(kbase[kk] + i), lane);
+                src[q] = (key == MAXP ? a.h_s : a.h_r) + (size_t)dest * Irows;
+                dst[q] = hq(kbase[kk] + i);
+                cidx[q] = 256 * ch;
+                nrow[q] = Irows;
+                act[q] = quant_load8<true>(src[q], Irows, cidx[q], lane, v[q]);
             }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (w0 + q * LW < ntask) quant_store8(v[q], act[q], nrow[q], cidx[q], dst[q], lane);
         }
         cbar();
         return m->bend;
@@ -554,10 +581,9 @@ struct LayerKernel {
     // of a tile always sees the full count (its own release came last); any
     // other block that also sees it writes the same values.
     __device__ void finish_tiles() {
-        if (warp == 0) {   // one fence for all o rows, then this block's tile tickets
-            __syncwarp();
+        cbar();   // every warp's o rows are ordered before warp 0's releases
+        if (warp == 0) {
             if (lane == 0) {
-                __threadfence();
                 for (int w = 0; w < 8; ++w) {
                     uint32_t bits = m->ytiles[w];
                     while (bits) {
@@ -723,11 +749,8 @@ struct LayerKernel {
             if (a.rbias) l = __fadd_rn(l, a.rbias[e0 + r]);
             a.logits[(size_t)t * a.E + e0 + r] = l;
         }
-        cbar();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            red_release(a.route_ctr, 1u);
-        }
+        cbar();   // orders the block's logit stores before thread 0's release
+        if (threadIdx.x == 0) red_release(a.route_ctr, 1u);
     }
 
     // k largest of E logits (largest first, lower index on equal logits) by one
@@ -1120,15 +1143,13 @@ struct LayerKernel {
 
     __device__ void finish() {
         if (threadIdx.x == 0) {
-            __threadfence();
             const unsigned old = atom_acqrel(a.done_ctr, 1u);
             if (old == (unsigned)G - 1u) {
                 *a.route_ctr = 0u;
                 for (int i = 0; i <= a.P; ++i) a.hctr[i] = 0u;
                 a.hctr[MAXP] = 0u;
                 for (int i = 0; i < a.H / 32; ++i) a.yticket[i] = 0u;
-                __threadfence();
-                *a.done_ctr = 0u;
+                *a.done_ctr = 0u;   // the next launch reads these after this grid completes
             }
         }
     }
