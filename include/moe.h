@@ -251,12 +251,13 @@ moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, con
  * (moe_route's fixed-order logits, top-k and gating) and the routed + shared
  * expert FFN (moe_expert_ffn's arithmetic), for decode where the three steps
  * sit back to back.  One persistent block per SM: every block quantises x and
- * computes the logits of its own router rows, a device-wide ticket publishes
- * the logits, each block selects the same top-k and streams its share of the
- * chosen experts' packed weights with TMA bulk copies into a shared-memory
- * ring; h and the per-tile slot sums are exchanged through the workspace with
- * release/acquire tickets.  Results equal those of the three calls (same
- * arithmetic and summation orders; y within rounding of moe_expert_ffn).
+ * computes the logits of its own router rows, every block reads all logits,
+ * selects the same top-k and streams its share of the chosen experts' packed
+ * weights with TMA bulk copies into a shared-memory ring.  Logits, h and the
+ * per-slot o rows pass between blocks through the workspace as 8-byte words
+ * that carry the value and a per-call epoch (a launch counter kept in the
+ * workspace), so readers poll the data itself.  Results equal those of the
+ * three calls (same arithmetic and summation orders).
  *   hidden      : device fp32 [T][H]; w_router/rtype/router_bias/k/gating/
  *                 renormalize as in moe_route; pool/shared as in moe_expert_ffn
  *                 (shared: the same format as pool or Q8_0)

@@ -13,9 +13,8 @@
 //     computes logits for its router rows in the fixed summation order and
 //     publishes them; while the other blocks finish, it runs its share of the
 //     shared expert's gate/up.
-//  3. A release/acquire ticket over all blocks makes every logit visible;
-//     each block selects the same top-k, groups the (token, slot) pairs by
-//     expert and derives the same work plan:
+//  3. Every block reads every logit and selects the same top-k, groups the
+//     (token, slot) pairs by expert and derives the same work plan:
 //       A units = (expert, 32-row tile of I): gate + up records,
 //       B units = (expert, 32-row tile of H): down records.
 //     A units are dealt out in a snake over blocks; B units are contiguous
@@ -23,14 +22,22 @@
 //  4. The producer streams each unit's records (TMA bulk copies, complete_tx
 //     mbarriers) through a byte ring; consumer warp r % 8 takes record r of a
 //     unit, so every sum has a fixed order whatever the batch.
-//  5. An A unit ends with h = silu(g) * u rows in global scratch and a
-//     release on its expert's ticket; a B unit first waits for the tickets of
-//     its expert, requantises that expert's h locally, and ends with o rows
-//     plus a ticket on its row tile; the block that completes a row tile sums
-//     the slots of each token in slot order (shared expert last) into y.
+//  5. An A unit ends with h = silu(g) * u rows in global scratch; a B unit's
+//     block first requantises its expert's h locally, and the unit ends with
+//     o rows; row tile rt of y is written by block rt % G, which sums the
+//     slots of each token in slot order (shared expert last).
+//  Exchanges between blocks (logits, h, o) carry no separate flag: every
+//  value is stored with this launch's epoch in one 8-byte word, and a reader
+//  polls the words it needs until they carry the epoch.  An 8-byte aligned
+//  access is single-copy atomic, so a word with the right epoch holds the
+//  right value and no fence is needed on either side.  The epoch is a counter
+//  in the workspace: read after the dependency wait, written back (+1) by
+//  block 0 at its end.
 //  Every wait is bounded (SM cycle counter); a timeout sets MOE_DEV_TIMEOUT,
 //  drains this block's copies in flight and returns.
 #pragma once
+
+#include <type_traits>
 
 #include "moe_common.cuh"
 #include "moe_launch.h"
@@ -40,6 +47,7 @@ namespace moe {
 constexpr int LW = 8;                  // consumer warps
 constexpr int LT = (LW + 1) * 32;      // threads per block (with the producer warp)
 constexpr int NBAR = 32;               // ring items in flight (barrier slots)
+constexpr int MAX_ITEM_RECS = 8;       // records per ring item, at most (also the empty-barrier count)
 // bound on every device-side wait, in SM clock cycles (about 0.4-1 s at the
 // clocks this part runs at); the cycle counter is cheap to poll
 constexpr long long WAIT_CYCLES = 800ll * 1000ll * 1000ll;
@@ -59,6 +67,9 @@ __device__ __forceinline__ void mbar_arm(uint64_t *b, uint32_t bytes) {
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_n(uint64_t *b, uint32_t n) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(n) : "memory");
 }
 __device__ __forceinline__ bool mbar_test(uint64_t *b, uint32_t parity) {
     uint32_t ok;
@@ -86,26 +97,30 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void red_release(unsigned *p, unsigned v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// tagged word: the value's bits in the low half, the epoch in the high half
+typedef unsigned long long tword;
+__device__ __forceinline__ void st_tag(tword *p, float v, uint32_t ep) {
+    const tword w = ((tword)ep << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
-__device__ __forceinline__ unsigned atom_acqrel(unsigned *p, unsigned v) {
-    unsigned o;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(o) : "l"(p), "r"(v) : "memory");
-    return o;
+__device__ __forceinline__ tword ld_tag(const tword *p) {
+    tword w;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
 }
-__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// two adjacent tagged words (16-byte aligned); each word is read atomically
+__device__ __forceinline__ void ld_tag2(const tword *p, tword &w0, tword &w1) {
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(p) : "memory");
+}
+__device__ __forceinline__ uint32_t tag_of(tword w) { return (uint32_t)(w >> 32); }
+__device__ __forceinline__ float tag_value(tword w) { return __uint_as_float((uint32_t)w); }
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const unsigned *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-// bounded spin until *p >= target; false on timeout
-__device__ __forceinline__ bool spin_geq(const unsigned *p, unsigned target) {
-    if (ld_acquire(p) >= target) return true;
-    const long long t0 = clock64();
-    while (ld_acquire(p) < target)
-        if (clock64() - t0 > WAIT_CYCLES) return false;
-    return true;
+__device__ __forceinline__ void st_relaxed_u32(unsigned *p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }   // consumers only
 
@@ -115,11 +130,9 @@ struct Misc {
     volatile int abort;
     int U, n_sa, n_ra, nA, n_sb, n_rb, nB, jb0, jb1;
     int tilesI, tilesIs, tilesH;
-    int nc;              // contributions per row tile of y
+    uint32_t ep;         // this launch's epoch
     uint32_t bitmap[MOE_MAX_EXPERTS / 32];
     int wpre[MOE_MAX_EXPERTS / 32];
-    uint32_t ytiles[8];  // row tiles of H this block contributed to (H <= 8192)
-    int hpend[MAXP + 1]; // h tiles this block wrote per expert, not yet released
     int nkeys, kkey[64], kslot[64];   // experts of the current B batch and their hq slots
     int bsnake, bp0, nb, bend;         // this block's B units: snake passes from bp0, or [jb0, jb1)
     unsigned long long bsum[LW], target, lo, hi;
@@ -150,6 +163,7 @@ struct LayerKernel {
     Smem o;
     Misc *m;
     int c, G, warp, lane;
+    uint32_t ep = 0;   // consumers: this launch's epoch (after the dependency wait)
 
     __device__ LayerKernel(const LayerArgs &args, unsigned char *smem) : a(args), sm(smem), o(args.sm) {
         m = reinterpret_cast<Misc *>(sm + o.misc);
@@ -181,20 +195,46 @@ struct LayerKernel {
     __device__ uint8_t *xq(int t) { return sm + o.xq + (size_t)t * a.xrec; }
     __device__ uint8_t *hq(int i) { return sm + o.hq + (size_t)i * a.hrec; }
 
-    __device__ void fail() {
+    // Slow paths are kept out of line: every launch runs this kernel's code
+    // once per phase, and instruction fetch of cold code costs about as much
+    // as the work, so each inlined copy of a rarely taken loop is paid for.
+    __device__ __noinline__ void fail() {
         m->abort = 1;
         atomicOr(a.status, MOE_DEV_TIMEOUT);
+    }
+
+    // p re-read until it carries this launch's epoch (bounded; on timeout the
+    // value is not used)
+    __device__ __noinline__ tword wait_tag_slow(const tword *p) {
+        const long long t0 = clock64();
+        for (;;) {
+            const tword w = ld_tag(p);
+            if (tag_of(w) == ep) return w;
+            if (m->abort || clock64() - t0 > WAIT_CYCLES) {
+                fail();
+                return w;
+            }
+        }
+    }
+    // w, already loaded from p, if it carries this launch's epoch, else p re-read
+    __device__ __forceinline__ tword wait_tag(const tword *p, tword w) {
+        return tag_of(w) == ep ? w : wait_tag_slow(p);
     }
 
     // ------------------------------------------------------------ units
     // kind: 0 shared A, 1 routed A, 2 shared B, 3 routed B
     struct Unit {
-        int kind, u, rt, nrec, nt;
+        int kind, u, rt, nrec, nt, nitems;
         const uint8_t *g, *up, *d;   // tile bases (A: gate/up, B: down)
         const moe_expert *ex;
     };
 
     __device__ void unit_of(int j, Unit &U) {
+        unit_of0(j, U);
+        const int R = U.kind <= 1 ? a.ra : a.rb;
+        U.nitems = (U.nrec + R - 1) / R;
+    }
+    __device__ void unit_of0(int j, Unit &U) {
         const moe_expert *T = table();
         if (j < m->n_sa) {
             U.kind = 0; U.u = MAXP; U.rt = j;
@@ -229,12 +269,23 @@ struct LayerKernel {
         }
     }
 
-    __device__ uint32_t item_bytes(const Unit &U, int r) {
+    // Ring item q of a unit: records [r0, r1) with r0 = q R (R = a.ra for A
+    // units, a.rb for B units).  An A item holds the gate run, then the up run
+    // of the same records; a B item holds the down run.
+    __device__ void item_recs(const Unit &U, int q, int &r0, int &r1) {
+        const int R = U.kind <= 1 ? a.ra : a.rb;
+        r0 = q * R;
+        r1 = min(r0 + R, U.nrec);
+    }
+    // byte offset of record r within its run (a run starts at record r0)
+    template <class FF>
+    __device__ static size_t run_off(int cols, int r0, int r) { return FF::rec_off(cols, r) - FF::rec_off(cols, r0); }
+    __device__ uint32_t run_bytes(const Unit &U, int r0, int r1) {
         switch (U.kind) {
-            case 0: return 2 * FS::rec_bytes(a.H, r);
-            case 1: return 2 * F::rec_bytes(a.H, r);
-            case 2: return FS::rec_bytes(a.Is, r);
-            default: return F::rec_bytes(a.I, r);
+            case 0: return (uint32_t)run_off<FS>(a.H, r0, r1);
+            case 1: return (uint32_t)run_off<F>(a.H, r0, r1);
+            case 2: return (uint32_t)run_off<FS>(a.Is, r0, r1);
+            default: return (uint32_t)run_off<F>(a.I, r0, r1);
         }
     }
 
@@ -271,8 +322,11 @@ struct LayerKernel {
         }
     }
 
-    __device__ bool issue(Ring &R, const Unit &U, int r) {
-        const uint32_t bytes = item_bytes(U, r);
+    __device__ bool issue(Ring &R, const Unit &U, int q) {
+        int r0, r1;
+        item_recs(U, q, r0, r1);
+        const uint32_t run = run_bytes(U, r0, r1);
+        const uint32_t bytes = U.kind <= 1 ? 2 * run : run;
         uint32_t start;
         if (!ring_place(R, bytes, start)) return false;
         const int i = R.issued;
@@ -281,14 +335,16 @@ struct LayerKernel {
         uint8_t *dst = sm + o.ring + start;
         uint64_t *fb = full_bar(i);
         mbar_arm(fb, bytes);
+        // consumers arrive once per record of an A item, once for a B item
+        const uint32_t users = U.kind <= 1 ? (uint32_t)(r1 - r0) : 1u;
+        if (users < MAX_ITEM_RECS) mbar_arrive_n(empty_bar(i), MAX_ITEM_RECS - users);
         if (U.kind == 0 || U.kind == 1) {
-            const uint32_t half = bytes / 2;
-            const size_t off = U.kind == 0 ? FS::rec_off(a.H, r) : F::rec_off(a.H, r);
-            bulk_g2s(dst, U.g + off, half, fb);
-            bulk_g2s(dst + half, U.up + off, half, fb);
+            const size_t off = U.kind == 0 ? FS::rec_off(a.H, r0) : F::rec_off(a.H, r0);
+            bulk_g2s(dst, U.g + off, run, fb);
+            bulk_g2s(dst + run, U.up + off, run, fb);
         } else {
-            const size_t off = U.kind == 2 ? FS::rec_off(a.Is, r) : F::rec_off(a.I, r);
-            bulk_g2s(dst, U.d + off, bytes, fb);
+            const size_t off = U.kind == 2 ? FS::rec_off(a.Is, r0) : F::rec_off(a.I, r0);
+            bulk_g2s(dst, U.d + off, run, fb);
         }
         R.head = start + bytes;
         ++R.issued;
@@ -298,9 +354,9 @@ struct LayerKernel {
     __device__ bool issue_unit(Ring &R, int j) {
         Unit U;
         unit_of(j, U);
-        for (int r = 0; r < U.nrec; ++r) {
+        for (int q = 0; q < U.nitems; ++q) {
             if (m->abort) return false;
-            if (!issue(R, U, r)) { fail(); return false; }
+            if (!issue(R, U, q)) { fail(); return false; }
         }
         return true;
     }
@@ -308,12 +364,17 @@ struct LayerKernel {
     // ------------------------------------------------------- consumers
     // one record of a unit: wait for it, pull it into registers, free the slot
     // wait for item i (a record, or a gate+up record pair) to land in the ring
+    // (a consumer ahead of the producer sleeps between polls of the tag: a
+    // tight loop of shared-memory loads by eight warps slows the producer's
+    // own shared-memory and barrier operations)
     __device__ const uint8_t *wait_item(int i) {
         if (m->abort) return nullptr;
         if (tags()[i % NBAR] != (uint32_t)i) {
             const long long t0 = clock64();
-            while (tags()[i % NBAR] != (uint32_t)i)
+            while (tags()[i % NBAR] != (uint32_t)i) {
+                __nanosleep(64);
                 if (clock64() - t0 > WAIT_CYCLES || m->abort) { fail(); return nullptr; }
+            }
         }
         if (!mbar_wait(full_bar(i), (uint32_t)((i / NBAR) & 1))) { fail(); return nullptr; }
         return sm + o.ring + starts()[i % NBAR];
@@ -333,10 +394,14 @@ struct LayerKernel {
 #pragma unroll
         for (int i = 0; i < NT; ++i)
             tok[i] = (i < U.nt) ? (U.kind == 0 ? i : plist()[uoff()[U.u] + i] / a.k) : 0;
-        for (int r = 0; r < U.nrec; ++r, ++item) {
-            if ((r & (LW - 1)) != warp) continue;
-            const uint8_t *rec = wait_item(item);
-            if (!rec) continue;
+        for (int r = warp; r < U.nrec; r += LW) {
+            int r0, r1;
+            item_recs(U, r / a.ra, r0, r1);
+            const int it = item + r / a.ra;
+            const uint8_t *base = wait_item(it);
+            if (!base) continue;
+            const uint8_t *rec = base + run_off<FF>(a.H, r0, r);
+            const uint8_t *rec_up = base + run_off<FF>(a.H, r0, r1) + run_off<FF>(a.H, r0, r);
             const int nb = FF::rec_blocks(a.H, r);
             const int k0 = r * FF::QK;
             {   // gate record, then up record: one record's registers live at a time
@@ -354,8 +419,8 @@ struct LayerKernel {
             }
             {
                 typename FF::W w;
-                FF::load_s(w, rec + FF::rec_bytes(a.H, r), nb, lane);
-                free_item(item);
+                FF::load_s(w, rec_up, nb, lane);
+                free_item(it);
 #pragma unroll
                 for (int i = 0; i < NT; ++i) {
                     if (i < U.nt) {
@@ -367,6 +432,7 @@ struct LayerKernel {
                 }
             }
         }
+        item += U.nitems;
         // NT <= 4: two reduction buffers alternate; NT = 16: one buffer, and
         // the barrier below keeps it until warp 0 has read the previous unit
         if (NT > 4) cbar();
@@ -380,7 +446,7 @@ struct LayerKernel {
         if (warp == 0) {
             const int row = U.rt * 32 + lane;
             const int Irows = U.kind == 0 ? a.Is : a.I;
-            float *hb = U.kind == 0 ? a.h_s : a.h_r;
+            tword *hb = U.kind == 0 ? a.h_s : a.h_r;
             for (int i = 0; i < U.nt && i < NT; ++i) {
                 float g = 0.f, uu = 0.f;
 #pragma unroll
@@ -392,31 +458,16 @@ struct LayerKernel {
                 if (U.ex->b_up) uu += U.ex->b_up[row];
                 const float h = g / (1.f + expf(-g)) * uu;
                 const int dest = U.kind == 0 ? i : plist()[uoff()[U.u] + i];
-                hb[(size_t)dest * Irows + row] = h;
+                st_tag(hb + (size_t)dest * Irows + row, h, ep);
             }
-            if (lane == 0) m->hpend[U.u] += 1;
         }
         rbuf ^= 1;
     }
 
-    // release the per-expert h tickets this block owes (its h rows were all
-    // written by warp 0); called by warp 0 after a run of A units
-    __device__ void release_h(int nrouted) {
-        __syncwarp();   // orders every lane's h stores before lane 0's releases
-        if (lane == 0) {
-            for (int u = -1; u < nrouted; ++u) {
-                const int key = u < 0 ? MAXP : u;
-                const int n = m->hpend[key];
-                if (n) { red_release(a.hctr + key, (unsigned)n); m->hpend[key] = 0; }
-            }
-        }
-        __syncwarp();
-    }
-
     // ---------------------------------------------------------- B phase
     // The block's B units run in batches of consecutive units whose experts'
-    // requantised h fit the hq buffer together.  Per batch: wait for those
-    // experts' h tickets (one lane per expert), requantise every pair of them
+    // requantised h fit the hq buffer together.  Per batch: read those
+    // experts' h (polling the tagged words) and requantise every pair of them
     // into hq (all warps), then unit b of the batch goes to warp b % 8, which
     // streams its records in order and writes the o rows itself.
 
@@ -429,8 +480,25 @@ struct LayerKernel {
 
     // From list entry n0, the longest run of B units whose distinct experts'
     // pairs fit the hq buffer together (at most 64 experts, chosen by thread
-    // 0): wait for those experts' h tickets and requantise their h into hq.
-    // Returns the end of the run.
+    // 0): requantise those experts' h into hq.  Returns the end of the run.
+    // lane's 8 h values (8 lane .. 8 lane + 7 of the 256-chunk at c0) from
+    // tagged words: four 16-byte loads, then a bounded re-read of any word
+    // that does not carry this launch's epoch yet; false past the row
+    __device__ bool load8_tagged(const tword *x, int n, int c0, float v[8]) {
+        const int e0 = c0 + 8 * lane;
+        if (e0 >= n || m->abort) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.f;
+            return false;
+        }
+        tword w[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ld_tag2(x + e0 + 2 * i, w[2 * i], w[2 * i + 1]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = tag_value(wait_tag(x + e0 + i, w[i]));
+        return true;
+    }
+
     __device__ int load_hq_batch(int n0, int nend) {
         int *kbase = m->kslot;
         int *keys = m->kkey;
@@ -453,14 +521,6 @@ struct LayerKernel {
         }
         cbar();
         const int nk = m->nkeys;
-        if (warp == 0 && !m->abort) {
-            for (int kk = lane; kk < nk; kk += 32) {
-                const int key = keys[kk];
-                const unsigned need = (unsigned)(key == MAXP ? m->tilesIs : m->tilesI);
-                if (!spin_geq(a.hctr + key, need)) fail();
-            }
-        }
-        cbar();
         const bool ok = !m->abort;
         // tasks (key, pair, 256-chunk), flattened; a warp loads the h of up to
         // four tasks before quantising them (each load is an L2 trip)
@@ -473,7 +533,7 @@ struct LayerKernel {
         for (int w0 = warp; ok && w0 < ntask; w0 += 4 * LW) {
             float v[4][8];
             bool act[4];
-            const float *src[4];
+            const tword *src[4];
             uint8_t *dst[4];
             int cidx[4], nrow[4];
 #pragma unroll
@@ -497,7 +557,7 @@ struct LayerKernel {
                 dst[q] = hq(kbase[kk] + i);
                 cidx[q] = 256 * ch;
                 nrow[q] = Irows;
-                act[q] = quant_load8<true>(src[q], Irows, cidx[q], lane, v[q]);
+                act[q] = load8_tagged(src[q], Irows, cidx[q], v[q]);
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -520,21 +580,25 @@ struct LayerKernel {
         float ao[NT];
 #pragma unroll
         for (int i = 0; i < NT; ++i) ao[i] = 0.f;
-        for (int r = 0; r < U.nrec; ++r, ++item) {
-            const uint8_t *rec = wait_item(item);
-            if (!rec) continue;
-            typename FF::W wd;
-            const int nb = FF::rec_blocks(Irows, r);
-            FF::load_s(wd, rec, nb, lane);
-            free_item(item);
-            const int k0 = r * FF::QK;
+        for (int q = 0; q < U.nitems; ++q) {
+            int r0, r1;
+            item_recs(U, q, r0, r1);
+            const uint8_t *base = wait_item(item + q);
+            if (!base) continue;
+            for (int r = r0; r < r1; ++r) {
+                typename FF::W wd;
+                const int nb = FF::rec_blocks(Irows, r);
+                FF::load_s(wd, base + run_off<FF>(Irows, r0, r), nb, lane);
+                if (r == r1 - 1) free_item(item + q);   // the item's last record is in registers
+                const int k0 = r * FF::QK;
 #pragma unroll
-            for (int i = 0; i < NT; ++i) {
-                if (i < U.nt) {
-                    const Act h = act_view(hq(slot0 + i), Irows);
-                    int is[FF::NSUB];
-                    FF::isums(wd, h, k0, nb, is);
-                    ao[i] = __fadd_rn(ao[i], FF::combine(wd, h, k0, nb, is));
+                for (int i = 0; i < NT; ++i) {
+                    if (i < U.nt) {
+                        const Act h = act_view(hq(slot0 + i), Irows);
+                        int is[FF::NSUB];
+                        FF::isums(wd, h, k0, nb, is);
+                        ao[i] = __fadd_rn(ao[i], FF::combine(wd, h, k0, nb, is));
+                    }
                 }
             }
         }
@@ -545,13 +609,12 @@ struct LayerKernel {
             if (i < U.nt) {
                 if (U.kind == 3) {
                     const int p = plist()[uoff()[U.u] + i];
-                    a.o_r[(size_t)p * a.H + row] = U.ex->b_down ? ao[i] + bd : ao[i];
+                    st_tag(a.o_r + (size_t)p * a.H + row, U.ex->b_down ? ao[i] + bd : ao[i], ep);
                 } else {
-                    a.o_s[(size_t)i * a.H + row] = ao[i];
+                    st_tag(a.o_s + (size_t)i * a.H + row, ao[i], ep);
                 }
             }
         }
-        if (lane == 0) atomicOr(&m->ytiles[U.rt >> 5], 1u << (U.rt & 31));
     }
 
     __device__ void run_B_phase(int &item) {
@@ -565,10 +628,10 @@ struct LayerKernel {
                 unit_of(b_unit(q), U);
                 if (((q - n) & (LW - 1)) == warp) {
                     const int slot = key_slot(U.kind == 2 ? MAXP : U.u);
-                    if (U.kind == 2) run_B_warp<FS>(U, it, slot);
-                    else run_B_warp<F>(U, it, slot);
+                    if (std::is_same<F, FS>::value || U.kind == 3) run_B_warp<F>(U, it, slot);
+                    else run_B_warp<FS>(U, it, slot);
                 }
-                it += U.nrec;
+                it += U.nitems;
             }
             item = it;
             cbar();   // the next batch overwrites hq
@@ -576,60 +639,40 @@ struct LayerKernel {
         }
     }
 
-    // After this block's B units: every row tile it contributed to whose
-    // ticket shows all contributions writes its y rows.  The last contributor
-    // of a tile always sees the full count (its own release came last); any
-    // other block that also sees it writes the same values.
+    // Row tile rt of y belongs to block rt % G; its n-th tile goes to warp
+    // n % 8.  Runs after the block's own B units.
     __device__ void finish_tiles() {
-        cbar();   // every warp's o rows are ordered before warp 0's releases
-        if (warp == 0) {
-            if (lane == 0) {
-                for (int w = 0; w < 8; ++w) {
-                    uint32_t bits = m->ytiles[w];
-                    while (bits) {
-                        red_release(a.yticket + 32 * w + __ffs(bits) - 1, 1u);
-                        bits &= bits - 1u;
-                    }
-                }
-            }
-            __syncwarp();
-        }
-        cbar();
         int n = 0;
-        for (int w = 0; w < 8; ++w) {
-            uint32_t bits = m->ytiles[w];
-            while (bits) {
-                const int rt = 32 * w + __ffs(bits) - 1;
-                bits &= bits - 1u;
-                if ((n++ % LW) != warp) continue;
-                unsigned v = 0;
-                if (lane == 0) v = ld_acquire(a.yticket + rt);
-                v = __shfl_sync(0xFFFFFFFFu, v, 0);
-                if (v >= (unsigned)m->nc) write_y(rt);
-            }
-        }
+        for (int rt = c; rt < a.H / 32; rt += G, ++n)
+            if ((n % LW) == warp) write_y(rt);
     }
 
     // y rows of one 32-row tile: slots in slot order, shared expert last.
-    // All loads of a token are issued before the sum (each is an L2 trip).
+    // A token's tagged o words are all loaded before any is waited on.
     __device__ void write_y(int rt) {
         const int row = rt * 32 + lane;
         for (int t = 0; t < a.T; ++t) {
             float y = 0.f;
             for (int s0 = 0; s0 < a.k; s0 += 8) {
-                float v[8];
+                tword w[8];
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) {
                     const int s = s0 + jj, p = t * a.k + s;
-                    v[jj] = (s < a.k && pu()[p] >= 0) ? __ldcg(a.o_r + (size_t)p * a.H + row) : 0.f;
+                    w[jj] = (s < a.k && pu()[p] >= 0) ? ld_tag(a.o_r + (size_t)p * a.H + row) : 0ull;
                 }
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) {
                     const int s = s0 + jj, p = t * a.k + s;
-                    if (s < a.k && pu()[p] >= 0) y += wts()[p] * v[jj];
+                    if (s < a.k && pu()[p] >= 0) {
+                        const float v = tag_value(wait_tag(a.o_r + (size_t)p * a.H + row, w[jj]));
+                        y += wts()[p] * v;
+                    }
                 }
             }
-            if (a.shared) y += __ldcg(a.o_s + (size_t)t * a.H + row);
+            if (a.shared) {
+                const tword *ps = a.o_s + (size_t)t * a.H + row;
+                y += tag_value(wait_tag(ps, ld_tag(ps)));
+            }
             a.y[(size_t)t * a.H + row] = y;
         }
     }
@@ -637,12 +680,12 @@ struct LayerKernel {
     // ------------------------------------------------------ phases
     __device__ void init() {
         if (threadIdx.x == 0) {
-            for (int i = 0; i < 2 * NBAR; ++i) mbar_init(reinterpret_cast<uint64_t *>(sm + o.bars) + i, 1);
+            for (int i = 0; i < NBAR; ++i) mbar_init(full_bar(i), 1);
+            for (int i = 0; i < NBAR; ++i) mbar_init(empty_bar(i), MAX_ITEM_RECS);
             mbar_init(fixed_bar(), 1);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             m->abort = 0;
         }
-        for (int i = threadIdx.x; i <= MAXP; i += LT) m->hpend[i] = 0;
         for (int i = threadIdx.x; i < NBAR; i += LT) tags()[i] = 0xFFFFFFFFu;
         __syncthreads();
     }
@@ -747,55 +790,84 @@ struct LayerKernel {
             float l = segv[(r * nseg) * a.T + t];
             for (int s = 1; s < nseg; ++s) l = __fadd_rn(l, segv[(r * nseg + s) * a.T + t]);
             if (a.rbias) l = __fadd_rn(l, a.rbias[e0 + r]);
-            a.logits[(size_t)t * a.E + e0 + r] = l;
+            st_tag(a.logits + (size_t)t * a.E + e0 + r, l, ep);
         }
-        cbar();   // orders the block's logit stores before thread 0's release
-        if (threadIdx.x == 0) red_release(a.route_ctr, 1u);
     }
 
     // k largest of E logits (largest first, lower index on equal logits) by one
     // warp: lane l holds keys of experts l + 32 j in registers; each round takes
-    // the warp maximum key, then the lowest index holding it.  Returns, in lane
-    // s < k, the s-th selected logit.
+    // the warp maximum key, then the lowest index holding it, and clears that
+    // key.  No branch depends on the data (rounds are unrolled for the usual
+    // k), which keeps the warp converged.  Writes the ids to out[0..k) and
+    // returns, in lane s < k, the s-th selected logit.
     template <int JN>
+    __device__ __forceinline__ void topk_round(uint32_t (&key)[JN], int s, int &myid, uint32_t &mykey) {
+        uint32_t best = key[0];
+        int bj = 0;
+#pragma unroll
+        for (int j = 1; j < JN; ++j) {
+            const bool more = key[j] > best;
+            best = more ? key[j] : best;
+            bj = more ? j : bj;
+        }
+        const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, best);
+        const int win = __reduce_min_sync(0xFFFFFFFFu, best == mx ? lane + 32 * bj : 0x7FFFFFFF);
+        const bool mine = (win & 31) == lane;
+#pragma unroll
+        for (int j = 0; j < JN; ++j) key[j] = (mine && j == bj) ? 0u : key[j];
+        myid = lane == s ? win : myid;
+        mykey = lane == s ? mx : mykey;
+    }
+    template <int JN, int K>
     __device__ float select_topk(const float *lg, int *out) {
-        uint32_t key[JN];
+        uint32_t key[JN];   // 0 marks padding (every real logit's key is > 0)
 #pragma unroll
         for (int j = 0; j < JN; ++j) {
             const int e = lane + 32 * j;
             key[j] = e < a.E ? fkey(lg[e]) : 0u;
         }
-        float mysel = 0.f;
-        for (int s = 0; s < a.k; ++s) {
-            uint32_t best = 0u;
-            int bj = 0;
+        int myid = 0;
+        uint32_t mykey = 0u;
+        if (K > 0) {
 #pragma unroll
-            for (int j = 0; j < JN; ++j)
-                if (key[j] > best) { best = key[j]; bj = j; }
-            const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, best);
-            const int cand = (best == mx && best != 0u) ? lane + 32 * bj : 0x7FFFFFFF;
-            const int win = __reduce_min_sync(0xFFFFFFFFu, cand);
-            if ((win & 31) == lane) {
-#pragma unroll
-                for (int j = 0; j < JN; ++j)
-                    if (j == (win >> 5)) key[j] = 0u;
-            }
-            if (lane == s) mysel = fkey_value(mx);
-            if (lane == 0) out[s] = win;
+            for (int s = 0; s < K; ++s) topk_round<JN>(key, s, myid, mykey);
+        } else {
+#pragma unroll 1
+            for (int s = 0; s < a.k; ++s) topk_round<JN>(key, s, myid, mykey);
         }
-        return mysel;
+        if (lane < a.k) out[lane] = myid;
+        return fkey_value(mykey);
+    }
+    template <int JN>
+    __device__ float select_topk_k(const float *lg, int *out) {
+        switch (a.k) {
+            case 8: return select_topk<JN, 8>(lg, out);
+            case 4: return select_topk<JN, 4>(lg, out);
+            case 2: return select_topk<JN, 2>(lg, out);
+            default: return select_topk<JN, 0>(lg, out);
+        }
     }
 
     __device__ void topk_and_group() {
-        if (threadIdx.x == 0 && !m->abort)
-            if (!spin_geq(a.route_ctr, (unsigned)G)) fail();
-        cbar();
         float *lgs = reinterpret_cast<float *>(sm + o.lg);
-        for (int i = threadIdx.x; i < a.T * a.E; i += LW * 32) lgs[i] = __ldcg(a.logits + i);
+        const int TE = a.T * a.E;
+        for (int i0 = threadIdx.x; i0 < TE; i0 += 4 * LW * 32) {
+            tword w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int i = i0 + q * LW * 32;
+                w[q] = i < TE ? ld_tag(a.logits + i) : 0ull;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int i = i0 + q * LW * 32;
+                if (i < TE) lgs[i] = tag_value(wait_tag(a.logits + i, w[q]));
+            }
+        }
         cbar();
         for (int t = warp; t < a.T; t += LW) {
             const float *lg = lgs + (size_t)t * a.E;
-            const float mysel = a.E <= 256 ? select_topk<8>(lg, ids() + t * a.k) : select_topk<32>(lg, ids() + t * a.k);
+            const float mysel = a.E <= 256 ? select_topk_k<8>(lg, ids() + t * a.k) : select_topk_k<32>(lg, ids() + t * a.k);
             if (lane < a.k) wts()[t * a.k + lane] = mysel;   // the weights replace these later
         }
         cbar();
@@ -952,7 +1024,6 @@ struct LayerKernel {
                 m->n_sb = a.shared ? m->tilesH : 0;
                 m->n_rb = m->U * m->tilesH;
                 m->nB = m->n_sb + m->n_rb;
-                m->nc = m->U + (a.shared ? 1 : 0);
                 m->bsnake = 1;
                 int p = 0;
                 while (snake_unit(p, c, G) < m->nA) ++p;
@@ -961,7 +1032,6 @@ struct LayerKernel {
                 while (snake_unit(p + n, c, G) < m->nA + m->nB) ++n;
                 m->nb = n;
             }
-            if (tid < 8) m->ytiles[tid] = 0u;
             cbar();
             return;
         }
@@ -976,11 +1046,9 @@ struct LayerKernel {
             m->n_sb = a.shared ? m->tilesH : 0;
             m->n_rb = m->U * m->tilesH;
             m->nB = m->n_sb + m->n_rb;
-            m->nc = m->U + (a.shared ? 1 : 0);
             const u64 tot = (u64)m->n_sa * sa + (u64)m->n_ra * ra + (u64)m->n_sb * sb + (u64)m->n_rb * rb;
             m->target = (u64)((float)tot / (float)G) + 1ull;   // any fixed rule works: all blocks agree
         }
-        if (tid < 8) m->ytiles[tid] = 0u;
         cbar();
         u64 my_a = 0;
         if (tid < G) {
@@ -1096,8 +1164,10 @@ struct LayerKernel {
 
     __device__ void consumer() {
         pdl_wait();
+        if (threadIdx.x == 0) m->ep = ld_relaxed_u32(a.epoch) + 1u;
         quantise_x();
         cbar();
+        ep = m->ep;
         if (c == 0 && a.xq_out) {
             const int n16 = (int)(a.xrec / 16);
             for (int i = threadIdx.x; i < a.T * n16; i += LW * 32)
@@ -1115,7 +1185,6 @@ struct LayerKernel {
                 run_A<FS>(U, item, rbuf);
             }
         }
-        if (warp == 0) release_h(0);
         topk_and_group();
         bar_handoff();
         gating_weights();
@@ -1128,30 +1197,20 @@ struct LayerKernel {
                 run_A<F>(U, item, rbuf);
             }
         }
-        if (warp == 0) release_h(m->U);
         // no loop below leaves early: every consumer thread must reach every
         // named barrier; after a timeout only waits and sums are skipped
         run_B_phase(item);
         finish_tiles();
-        if (m->nB == 0 && c == 0) {   // nothing owned: y = 0
-            for (int i = threadIdx.x; i < a.T * a.H; i += LW * 32) a.y[i] = 0.f;
-        }
     }
 
     // the handoff barrier pairs with the producer's __syncthreads
     __device__ void bar_handoff() { __syncthreads(); }
 
+    // block 0 advances the epoch once it is done: every block read it before
+    // publishing its logits, which block 0 has consumed; the next launch reads
+    // it after this grid has completed
     __device__ void finish() {
-        if (threadIdx.x == 0) {
-            const unsigned old = atom_acqrel(a.done_ctr, 1u);
-            if (old == (unsigned)G - 1u) {
-                *a.route_ctr = 0u;
-                for (int i = 0; i <= a.P; ++i) a.hctr[i] = 0u;
-                a.hctr[MAXP] = 0u;
-                for (int i = 0; i < a.H / 32; ++i) a.yticket[i] = 0u;
-                *a.done_ctr = 0u;   // the next launch reads these after this grid completes
-            }
-        }
+        if (c == 0 && threadIdx.x == 0) st_relaxed_u32(a.epoch, m->ep);
     }
 };
 

@@ -21,34 +21,40 @@ LayerWs layer_ws_layout(int T, int k, int H, int I, int Is, int E) {
     const size_t P = (size_t)T * k;
     LayerWs w;
     w.status = 0;
-    w.route_ctr = 64;
-    w.done_ctr = 128;
-    w.hctr = 256;
-    w.yticket = al(w.hctr + 4 * (size_t)(MAXP + 1));
-    w.logits = al(w.yticket + 4 * (size_t)(H / 32));
-    w.h_r = al(w.logits + 4 * (size_t)T * E);
-    w.h_s = al(w.h_r + 4 * P * I);
-    w.o_r = al(w.h_s + 4 * (size_t)T * (Is > 0 ? Is : 0));
-    w.o_s = al(w.o_r + 4 * P * H);
-    w.total = al(w.o_s + 4 * (size_t)T * H);
+    w.epoch = 64;
+    w.logits = 256;
+    w.h_r = al(w.logits + 8 * (size_t)T * E);
+    w.h_s = al(w.h_r + 8 * P * I);
+    w.o_r = al(w.h_s + 8 * (size_t)T * (Is > 0 ? Is : 0));
+    w.o_s = al(w.o_r + 8 * P * H);
+    w.total = al(w.o_s + 8 * (size_t)T * H);
     return w;
 }
 
-// largest ring item of a format: a gate+up record pair, or one down record
-static uint32_t max_item(int q, int H, int I) {
-    auto rec = [](int qq, int cols) -> uint32_t {
-        switch (qq) {
-            case MOE_Q4_K: return 9 * 512;
-            case MOE_Q2_K: return 5 * 512 + 128;
-            case MOE_Q8_0: return 17 * 512;
-            default: {
-                const int nb = cols / 32 < 8 ? cols / 32 : 8;
-                return (uint32_t)nb * 512 + 256;
-            }
+// largest packed record of a format for rows of `cols` columns
+static uint32_t max_rec(int q, int cols) {
+    switch (q) {
+        case MOE_Q4_K: return 9 * 512;
+        case MOE_Q2_K: return 5 * 512 + 128;
+        case MOE_Q8_0: return 17 * 512;
+        default: {
+            const int nb = cols / 32 < 8 ? cols / 32 : 8;
+            return (uint32_t)nb * 512 + 256;
         }
-    };
-    const uint32_t a = 2 * rec(q, H), b = rec(q, I);
+    }
+}
+// smallest possible ring item of a format: a gate+up record pair, or one down record
+static uint32_t max_item(int q, int H, int I) {
+    const uint32_t a = 2 * max_rec(q, H), b = max_rec(q, I);
     return a > b ? a : b;
+}
+// records per ring item: as many as keep an item within a quarter of the ring
+// (fewer, larger copies land sooner), between 1 and 8
+static int recs_per_item(size_t ring, uint32_t rec_bytes) {
+    size_t r = ring / 4 / rec_bytes;
+    if (r < 1) r = 1;
+    if (r > 8) r = 8;
+    return (int)r;
 }
 
 cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStream_t s) {
@@ -100,6 +106,16 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
     if (ring < 2 * (size_t)item) ring = 2 * (size_t)item;
     if (fixed_rest + ring > optin) ring = (optin - fixed_rest) & ~(size_t)127;
     a.ring_bytes = (uint32_t)ring;
+    {
+        uint32_t pa = 2 * max_rec(qtype, a.H), pb = max_rec(qtype, a.I);
+        if (a.shared) {
+            const uint32_t sa = 2 * max_rec(sqtype, a.H), sb = max_rec(sqtype, a.Is);
+            if (sa > pa) pa = sa;
+            if (sb > pb) pb = sb;
+        }
+        a.ra = recs_per_item(ring, pa);
+        a.rb = recs_per_item(ring, pb);
+    }
     o.ring = take(ring);
     o.bars = take((2 * kNBAR + 1) * 8);
     o.starts = take(2 * kNBAR * 4);   // item start offsets, then slot tags
@@ -179,15 +195,13 @@ moe_status moe_layer_forward(const float *hidden, int T, const void *w_router, m
     a.logits_out = logits_out;
     a.xq_out = (uint8_t *)xq_out;
     a.status = (unsigned *)(w + L.status);
-    a.route_ctr = (unsigned *)(w + L.route_ctr);
-    a.done_ctr = (unsigned *)(w + L.done_ctr);
-    a.hctr = (unsigned *)(w + L.hctr);
-    a.yticket = (unsigned *)(w + L.yticket);
-    a.logits = (float *)(w + L.logits);
-    a.h_r = (float *)(w + L.h_r);
-    a.h_s = (float *)(w + L.h_s);
-    a.o_r = (float *)(w + L.o_r);
-    a.o_s = (float *)(w + L.o_s);
+    a.epoch = (unsigned *)(w + L.epoch);
+    typedef unsigned long long tw;
+    a.logits = (tw *)(w + L.logits);
+    a.h_r = (tw *)(w + L.h_r);
+    a.h_s = (tw *)(w + L.h_s);
+    a.o_r = (tw *)(w + L.o_r);
+    a.o_s = (tw *)(w + L.o_s);
     a.rtype = rtype;
     a.k = k;
     a.gating = gating;

@@ -59,19 +59,22 @@ struct LayerArgs {
     float *w_out;
     float *logits_out;
     uint8_t *xq_out;
-    unsigned *status, *route_ctr, *done_ctr, *hctr, *yticket;   // workspace
-    float *logits, *h_r, *h_s, *o_r, *o_s;
+    unsigned *status, *epoch;       // workspace: status word, launch counter
+    // tagged words (value bits | epoch << 32): logits [T][E], h [T*k][I],
+    // shared h [T][Is], o [T*k][H], shared o [T][H]
+    unsigned long long *logits, *h_r, *h_s, *o_r, *o_s;
     int rtype, k, gating, renorm;
     int T, H, I, Is, E, P, NT;
     int table_in_smem;
     int hq_slots;                   // q8 records of requantised h the block can hold
     uint32_t ring_bytes;
+    int ra, rb;                     // records per ring item: A (gate + up runs), B (down run)
     size_t xrec, hrec;
     Smem sm;
 };
 
 struct LayerWs {
-    size_t status, route_ctr, done_ctr, hctr, yticket, logits, h_r, h_s, o_r, o_s, total;
+    size_t status, epoch, logits, h_r, h_s, o_r, o_s, total;
 };
 LayerWs layer_ws_layout(int T, int k, int H, int I, int Is, int E);
 // plans shared memory and launches the fused layer kernel for the pool's formats
