@@ -80,13 +80,15 @@ __device__ __forceinline__ bool mbar_test(uint64_t *b, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// bounded wait on an mbarrier phase; false on timeout
-__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity) {
-    if (mbar_test(b, parity)) return true;
+// bounded wait on an mbarrier phase; false on timeout (the loop is out of line)
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *b, uint32_t parity) {
     const long long t0 = clock64();
     while (!mbar_test(b, parity))
         if (clock64() - t0 > WAIT_CYCLES) return false;
     return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity) {
+    return mbar_test(b, parity) || mbar_wait_slow(b, parity);
 }
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile(
@@ -139,6 +141,41 @@ struct Misc {
 };
 
 static_assert(sizeof(Misc) <= kLayerMiscBytes, "fused kernel block state outgrew its shared-memory region");
+
+// Slow paths, out of line and free of the kernel object: every launch runs
+// this kernel's code once per phase, and fetching cold instructions costs
+// about as much as the work, so each inlined copy of a rarely taken loop is
+// paid for on every launch.
+static __device__ __noinline__ void fail_dev(Misc *m, unsigned *status) {
+    m->abort = 1;
+    atomicOr(status, MOE_DEV_TIMEOUT);
+}
+// p re-read until it carries epoch ep (bounded; on timeout the value is not used)
+static __device__ __noinline__ tword wait_tag_slow(const tword *p, uint32_t ep, Misc *m, unsigned *status) {
+    const long long t0 = clock64();
+    for (;;) {
+        const tword w = ld_tag(p);
+        if (tag_of(w) == ep) return w;
+        if (m->abort || clock64() - t0 > WAIT_CYCLES) {
+            fail_dev(m, status);
+            return w;
+        }
+    }
+}
+// ring item i: its slot tag set by the producer (a consumer ahead of the
+// producer sleeps between polls: a tight loop of shared-memory loads by eight
+// warps slows the producer), then its full barrier; false on abort or timeout
+static __device__ __noinline__ bool wait_item_slow(int i, volatile uint32_t *tags, uint64_t *full, Misc *m,
+                                                   unsigned *status) {
+    if (m->abort) return false;
+    const long long t0 = clock64();
+    while (tags[i % NBAR] != (uint32_t)i) {
+        __nanosleep(64);
+        if (clock64() - t0 > WAIT_CYCLES || m->abort) { fail_dev(m, status); return false; }
+    }
+    if (!mbar_wait(full, (uint32_t)((i / NBAR) & 1))) { fail_dev(m, status); return false; }
+    return true;
+}
 
 // monotone unsigned key of a float (larger float -> larger key); -0 and +0
 // share the key of +0 so equal logits tie and the lower index wins
@@ -195,30 +232,11 @@ struct LayerKernel {
     __device__ uint8_t *xq(int t) { return sm + o.xq + (size_t)t * a.xrec; }
     __device__ uint8_t *hq(int i) { return sm + o.hq + (size_t)i * a.hrec; }
 
-    // Slow paths are kept out of line: every launch runs this kernel's code
-    // once per phase, and instruction fetch of cold code costs about as much
-    // as the work, so each inlined copy of a rarely taken loop is paid for.
-    __device__ __noinline__ void fail() {
-        m->abort = 1;
-        atomicOr(a.status, MOE_DEV_TIMEOUT);
-    }
+    __device__ void fail() { fail_dev(m, a.status); }
 
-    // p re-read until it carries this launch's epoch (bounded; on timeout the
-    // value is not used)
-    __device__ __noinline__ tword wait_tag_slow(const tword *p) {
-        const long long t0 = clock64();
-        for (;;) {
-            const tword w = ld_tag(p);
-            if (tag_of(w) == ep) return w;
-            if (m->abort || clock64() - t0 > WAIT_CYCLES) {
-                fail();
-                return w;
-            }
-        }
-    }
     // w, already loaded from p, if it carries this launch's epoch, else p re-read
     __device__ __forceinline__ tword wait_tag(const tword *p, tword w) {
-        return tag_of(w) == ep ? w : wait_tag_slow(p);
+        return tag_of(w) == ep ? w : wait_tag_slow(p, ep, m, a.status);
     }
 
     // ------------------------------------------------------------ units
@@ -367,17 +385,10 @@ struct LayerKernel {
     // (a consumer ahead of the producer sleeps between polls of the tag: a
     // tight loop of shared-memory loads by eight warps slows the producer's
     // own shared-memory and barrier operations)
-    __device__ const uint8_t *wait_item(int i) {
-        if (m->abort) return nullptr;
-        if (tags()[i % NBAR] != (uint32_t)i) {
-            const long long t0 = clock64();
-            while (tags()[i % NBAR] != (uint32_t)i) {
-                __nanosleep(64);
-                if (clock64() - t0 > WAIT_CYCLES || m->abort) { fail(); return nullptr; }
-            }
-        }
-        if (!mbar_wait(full_bar(i), (uint32_t)((i / NBAR) & 1))) { fail(); return nullptr; }
-        return sm + o.ring + starts()[i % NBAR];
+    __device__ __forceinline__ const uint8_t *wait_item(int i) {
+        const bool ok = (!m->abort && tags()[i % NBAR] == (uint32_t)i && mbar_test(full_bar(i), (uint32_t)((i / NBAR) & 1))) ||
+                        wait_item_slow(i, tags(), full_bar(i), m, a.status);
+        return ok ? sm + o.ring + starts()[i % NBAR] : nullptr;
     }
     __device__ void free_item(int i) {
         __syncwarp();
@@ -523,21 +534,21 @@ struct LayerKernel {
         const int nk = m->nkeys;
         const bool ok = !m->abort;
         // tasks (key, pair, 256-chunk), flattened; a warp loads the h of up to
-        // four tasks before quantising them (each load is an L2 trip)
+        // two tasks before quantising them (each load is an L2 trip)
         int ntask = 0;
         for (int kk = 0; kk < nk; ++kk) {
             const int key = keys[kk];
             const int Irows = key == MAXP ? a.Is : a.I;
             ntask += key_pairs(key) * ((Irows + 255) / 256);
         }
-        for (int w0 = warp; ok && w0 < ntask; w0 += 4 * LW) {
-            float v[4][8];
-            bool act[4];
-            const tword *src[4];
-            uint8_t *dst[4];
-            int cidx[4], nrow[4];
+        for (int w0 = warp; ok && w0 < ntask; w0 += 2 * LW) {
+            float v[2][8];
+            bool act[2];
+            const tword *src[2];
+            uint8_t *dst[2];
+            int cidx[2], nrow[2];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
                 const int w = w0 + q * LW;
                 act[q] = false;
                 if (w >= ntask) continue;
@@ -560,7 +571,7 @@ struct LayerKernel {
                 act[q] = load8_tagged(src[q], Irows, cidx[q], v[q]);
             }
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 2; ++q)
                 if (w0 + q * LW < ntask) quant_store8(v[q], act[q], nrow[q], cidx[q], dst[q], lane);
         }
         cbar();
