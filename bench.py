@@ -49,6 +49,33 @@ def parse():
     return p.parse_args()
 
 
+def rank_env():
+    """(rank, world size, local rank) from the torchrun environment; (0, 1, 0) alone."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Seed of a rank's tokens: every rank decodes its own tokens (data parallel)."""
+    return seed + 7919 * rank
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest value over all ranks (the slowest rank sets the job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, layers: int, tokens: int, seconds: float) -> float:
+    """Layer-tokens per second of the whole job: every rank processed steps x layers x tokens."""
+    return world * steps * layers * tokens / seconds
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -189,9 +216,7 @@ def main():
     import synth
     cfg = synth.CONFIGS[args.config]
     L = args.layers or DEFAULT_LAYERS.get(args.config, cfg.layers)
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local = rank_env()
     if args.impl == "reference":
         return run_reference(args, cfg, L, rank, world)
 
@@ -212,7 +237,7 @@ def main():
     t_gen = time.perf_counter()
     layers, host_sample = [], []
     for l in range(L):
-        Lh = synth.make_layer(cfg, l, T=T, seed=args.seed + 7919 * rank)
+        Lh = synth.make_layer(cfg, l, T=T, seed=rank_seed(args.seed, rank))
         layers.append(DeviceLayer(Lh, dev))
         if l < 2 and rank == 0 and not args.no_cpu:
             host_sample.append(Lh)
@@ -276,12 +301,7 @@ def main():
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(e0.elapsed_time(e1), world, dev)
 
     K, W = args.steps, max(3, args.warmup)
     with ClockSampler(local) as cs:
@@ -312,16 +332,12 @@ def main():
                 graphs["step"].replay()
                 ys.copy_(Y, non_blocking=True)
                 stream.synchronize()
-        dt = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([dt], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dt = float(t.item())
-        e2e = {"value": world * ke * L * T / dt, "unit": UNIT, "h2d_bytes_per_step": L * T * cfg.H * 4,
+        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": job_throughput(world, ke, L, T, dt), "unit": UNIT, "h2d_bytes_per_step": L * T * cfg.H * 4,
                "d2h_bytes_per_step": L * T * cfg.H * 4, "steps": ke,
                "mode": "pinned H2D + graph replay of the public C-ABI calls + D2H + stream sync, wall clock"}
 
-    value = world * K * L * T / (ms / 1e3)
+    value = job_throughput(world, K, L, T, ms / 1e3)
     peak, peak_src = peaks()
     launch_ms = ms / (K * L)
     achieved = (step_bytes / L) / (launch_ms / 1e3) / 1e9
