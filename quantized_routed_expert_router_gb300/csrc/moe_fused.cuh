@@ -133,10 +133,15 @@ struct Misc {
     int U, n_sa, n_ra, nA, n_sb, n_rb, nB, jb0, jb1;
     int tilesI, tilesIs, tilesH;
     uint32_t ep;         // this launch's epoch
+    moe_expert shx;      // the shared expert's table entry, copied before the routing handoff
     uint32_t bitmap[MOE_MAX_EXPERTS / 32];
     int wpre[MOE_MAX_EXPERTS / 32];
     int nkeys, kkey[64], kslot[64];   // experts of the current B batch and their hq slots
     int bsnake, bp0, nb, bend;         // this block's B units: snake passes from bp0, or [jb0, jb1)
+    // the current hq batch's B units (at most 64): unit index, first ring
+    // item and first record (relative to the batch; entry [n] holds the
+    // totals) and hq slot
+    int bt_j[64], bt_it[65], bt_rec[65], bt_slot[64];
     unsigned long long bsum[LW], target, lo, hi;
 };
 
@@ -162,6 +167,35 @@ static __device__ __noinline__ tword wait_tag_slow(const tword *p, uint32_t ep, 
         }
     }
 }
+// words[q] (q < n) were loaded from base + q * stride; re-read, in rounds that
+// issue every load still needed at once, until all carry epoch ep (bounded;
+// on timeout the values are not used).  One round trip per round rather than
+// one per word.
+template <int N>
+static __device__ __noinline__ void wait_tags_slow(const tword *base, int stride, int n, tword *words, uint32_t ep,
+                                                  Misc *m, unsigned *status) {
+    tword w[N];
+#pragma unroll
+    for (int q = 0; q < N; ++q) w[q] = q < n ? words[q] : ((tword)ep << 32);
+    const long long t0 = clock64();
+    for (;;) {
+#pragma unroll
+        for (int q = 0; q < N; ++q)
+            if (tag_of(w[q]) != ep) w[q] = ld_tag(base + (size_t)q * stride);
+        bool all = true;
+#pragma unroll
+        for (int q = 0; q < N; ++q) all &= tag_of(w[q]) == ep;
+        if (all) break;
+        if (m->abort || clock64() - t0 > WAIT_CYCLES) {
+            fail_dev(m, status);
+            break;
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < N; ++q)
+        if (q < n) words[q] = w[q];
+}
+
 // ring item i: its slot tag set by the producer (a consumer ahead of the
 // producer sleeps between polls: a tight loop of shared-memory loads by eight
 // warps slows the producer), then its full barrier; false on abort or timeout
@@ -177,6 +211,31 @@ static __device__ __noinline__ bool wait_item_slow(int i, volatile uint32_t *tag
     return true;
 }
 
+// Compute steps shared by several phases.
+//
+// The block's dynamic shared memory.  Code that gets byte offsets into it
+// (rather than generic pointers) compiles to shared-memory loads.
+extern __shared__ __align__(128) unsigned char moe_smem[];
+
+// One packed record (at shared offset rec) dotted with nt activation records
+// (record i at shared offset abase + aidx[i] * astride): integer sub-block
+// dots, accumulated in record order into acc[i].  Used by the gate, up and
+// down projections.
+template <class FF, int NT>
+static __device__ __forceinline__ void rec_dot(uint32_t rec, int nb, int k0, int cols, uint32_t abase, uint32_t astride,
+                                            const int *aidx, int nt, int lane, float *acc) {
+    typename FF::W w;
+    FF::load_s(w, moe_smem + rec, nb, lane);
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+        if (i < nt) {
+            const Act x = act_view(moe_smem + abase + (uint32_t)aidx[i] * astride, cols);
+            int is[FF::NSUB];
+            FF::isums(w, x, k0, nb, is);
+            acc[i] = __fadd_rn(acc[i], FF::combine(w, x, k0, nb, is));
+        }
+    }
+}
 // monotone unsigned key of a float (larger float -> larger key); -0 and +0
 // share the key of +0 so equal logits tie and the lower index wins
 __device__ __forceinline__ uint32_t fkey(float v) {
@@ -193,6 +252,24 @@ __device__ __forceinline__ int snake_unit(int pass, int c, int G) {
     return pass * G + ((pass & 1) ? (G - 1 - c) : c);
 }
 
+// The work plan every thread keeps in registers once it is known (thread 0
+// derives it in shared memory; re-reading those words and dividing by the
+// tile counts on every use cost hundreds of cycles per unit).
+struct Plan {
+    int n_sa, nA, n_sb, nB;      // A units: shared then routed; B units: shared then routed
+    int tilesI, tilesIs, tilesH; // 32-row tiles of I, of the shared expert's I, of H
+    float invI, invH;            // 1 / tilesI, 1 / tilesH (quotients corrected exactly)
+    int bsnake, bp0, nb, jb0;    // this block's B units: snake passes from bp0, or [jb0, jb0 + nb)
+};
+
+// q / t for 0 <= q < 2^22, t >= 1, from a float estimate corrected exactly
+__device__ __forceinline__ int div_tiles(int q, int t, float inv) {
+    int u = (int)((float)q * inv);
+    if (u * t > q) --u;
+    if ((u + 1) * t <= q) ++u;
+    return u;
+}
+
 template <class F, class FS, int NT>
 struct LayerKernel {
     const LayerArgs &a;
@@ -201,6 +278,10 @@ struct LayerKernel {
     Misc *m;
     int c, G, warp, lane;
     uint32_t ep = 0;   // consumers: this launch's epoch (after the dependency wait)
+    Plan p;            // loaded by load_plan once the plan is in shared memory
+    // the shared expert's table entry: the caller's device table until the
+    // routing handoff, then the block's shared-memory copy of it
+    const moe_expert *shp;
 
     __device__ LayerKernel(const LayerArgs &args, unsigned char *smem) : a(args), sm(smem), o(args.sm) {
         m = reinterpret_cast<Misc *>(sm + o.misc);
@@ -208,6 +289,7 @@ struct LayerKernel {
         G = gridDim.x;
         warp = threadIdx.x >> 5;
         lane = threadIdx.x & 31;
+        shp = args.shared;
     }
 
     __device__ uint64_t *full_bar(int i) { return reinterpret_cast<uint64_t *>(sm + o.bars) + (i % NBAR); }
@@ -234,9 +316,33 @@ struct LayerKernel {
 
     __device__ void fail() { fail_dev(m, a.status); }
 
+    __device__ void load_plan() {
+        p.n_sa = m->n_sa;
+        p.nA = m->nA;
+        p.n_sb = m->n_sb;
+        p.nB = m->nB;
+        p.tilesI = a.I / 32;
+        p.tilesIs = a.shared ? a.Is / 32 : 0;
+        p.tilesH = a.H / 32;
+        p.invI = 1.f / (float)p.tilesI;
+        p.invH = 1.f / (float)p.tilesH;
+        p.bsnake = m->bsnake;
+        p.bp0 = m->bp0;
+        p.nb = m->nb;
+        p.jb0 = m->jb0;
+    }
+
     // w, already loaded from p, if it carries this launch's epoch, else p re-read
     __device__ __forceinline__ tword wait_tag(const tword *p, tword w) {
         return tag_of(w) == ep ? w : wait_tag_slow(p, ep, m, a.status);
+    }
+    // n <= 8 words loaded from base + q * stride: all of them with this epoch
+    __device__ __forceinline__ void wait_tags(const tword *base, int stride, int n, tword *w) {
+        bool all = true;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (q < n) all &= tag_of(w[q]) == ep;
+        if (!all) wait_tags_slow<8>(base, stride, n, w, ep, m, a.status);
     }
 
     // ------------------------------------------------------------ units
@@ -249,37 +355,37 @@ struct LayerKernel {
 
     __device__ void unit_of(int j, Unit &U) {
         unit_of0(j, U);
-        const int R = U.kind <= 1 ? a.ra : a.rb;
-        U.nitems = (U.nrec + R - 1) / R;
+        const int lg = U.kind <= 1 ? a.lgra : a.lgrb;
+        U.nitems = (U.nrec + (1 << lg) - 1) >> lg;
     }
     __device__ void unit_of0(int j, Unit &U) {
         const moe_expert *T = table();
-        if (j < m->n_sa) {
+        if (j < p.n_sa) {
             U.kind = 0; U.u = MAXP; U.rt = j;
-            U.ex = a.shared;
+            U.ex = shp;
             U.nrec = FS::nrec(a.H);
             U.nt = a.T;
             const size_t tb = FS::tile_bytes(a.H);
-            U.g = (const uint8_t *)a.shared->gate + (size_t)U.rt * tb;
-            U.up = (const uint8_t *)a.shared->up + (size_t)U.rt * tb;
-        } else if (j < m->nA) {
-            const int q = j - m->n_sa;
-            U.kind = 1; U.u = q / m->tilesI; U.rt = q - U.u * m->tilesI;
+            U.g = (const uint8_t *)shp->gate + (size_t)U.rt * tb;
+            U.up = (const uint8_t *)shp->up + (size_t)U.rt * tb;
+        } else if (j < p.nA) {
+            const int q = j - p.n_sa;
+            U.kind = 1; U.u = div_tiles(q, p.tilesI, p.invI); U.rt = q - U.u * p.tilesI;
             U.ex = T + ue()[U.u];
             U.nrec = F::nrec(a.H);
             U.nt = uoff()[U.u + 1] - uoff()[U.u];
             const size_t tb = F::tile_bytes(a.H);
             U.g = (const uint8_t *)U.ex->gate + (size_t)U.rt * tb;
             U.up = (const uint8_t *)U.ex->up + (size_t)U.rt * tb;
-        } else if (j < m->nA + m->n_sb) {
-            U.kind = 2; U.u = MAXP; U.rt = j - m->nA;
-            U.ex = a.shared;
+        } else if (j < p.nA + p.n_sb) {
+            U.kind = 2; U.u = MAXP; U.rt = j - p.nA;
+            U.ex = shp;
             U.nrec = FS::nrec(a.Is);
             U.nt = a.T;
-            U.d = (const uint8_t *)a.shared->down + (size_t)U.rt * FS::tile_bytes(a.Is);
+            U.d = (const uint8_t *)shp->down + (size_t)U.rt * FS::tile_bytes(a.Is);
         } else {
-            const int q = j - m->nA - m->n_sb;
-            U.kind = 3; U.u = q / m->tilesH; U.rt = q - U.u * m->tilesH;
+            const int q = j - p.nA - p.n_sb;
+            U.kind = 3; U.u = div_tiles(q, p.tilesH, p.invH); U.rt = q - U.u * p.tilesH;
             U.ex = T + ue()[U.u];
             U.nrec = F::nrec(a.I);
             U.nt = uoff()[U.u + 1] - uoff()[U.u];
@@ -287,13 +393,13 @@ struct LayerKernel {
         }
     }
 
-    // Ring item q of a unit: records [r0, r1) with r0 = q R (R = a.ra for A
-    // units, a.rb for B units).  An A item holds the gate run, then the up run
+    // Ring item q of a unit: records [r0, r1) with r0 = q R (R = 2^a.lgra for
+    // A units, 2^a.lgrb for B units).  An A item holds the gate run, then the up run
     // of the same records; a B item holds the down run.
     __device__ void item_recs(const Unit &U, int q, int &r0, int &r1) {
-        const int R = U.kind <= 1 ? a.ra : a.rb;
-        r0 = q * R;
-        r1 = min(r0 + R, U.nrec);
+        const int lg = U.kind <= 1 ? a.lgra : a.lgrb;
+        r0 = q << lg;
+        r1 = min(r0 + (1 << lg), U.nrec);
     }
     // byte offset of record r within its run (a run starts at record r0)
     template <class FF>
@@ -353,8 +459,8 @@ struct LayerKernel {
         uint8_t *dst = sm + o.ring + start;
         uint64_t *fb = full_bar(i);
         mbar_arm(fb, bytes);
-        // consumers arrive once per record of an A item, once for a B item
-        const uint32_t users = U.kind <= 1 ? (uint32_t)(r1 - r0) : 1u;
+        // consumers arrive once per record of the item
+        const uint32_t users = (uint32_t)(r1 - r0);
         if (users < MAX_ITEM_RECS) mbar_arrive_n(empty_bar(i), MAX_ITEM_RECS - users);
         if (U.kind == 0 || U.kind == 1) {
             const size_t off = U.kind == 0 ? FS::rec_off(a.H, r0) : F::rec_off(a.H, r0);
@@ -390,9 +496,10 @@ struct LayerKernel {
                         wait_item_slow(i, tags(), full_bar(i), m, a.status);
         return ok ? sm + o.ring + starts()[i % NBAR] : nullptr;
     }
-    __device__ void free_item(int i) {
+    // n consumer arrivals on item i's empty barrier (one per record used)
+    __device__ void free_item(int i, uint32_t n = 1) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(i));
+        if (lane == 0) mbar_arrive_n(empty_bar(i), n);
     }
 
     // A unit: g and u partial sums of this warp's records, then h rows
@@ -407,41 +514,17 @@ struct LayerKernel {
             tok[i] = (i < U.nt) ? (U.kind == 0 ? i : plist()[uoff()[U.u] + i] / a.k) : 0;
         for (int r = warp; r < U.nrec; r += LW) {
             int r0, r1;
-            item_recs(U, r / a.ra, r0, r1);
-            const int it = item + r / a.ra;
+            item_recs(U, r >> a.lgra, r0, r1);
+            const int it = item + (r >> a.lgra);
             const uint8_t *base = wait_item(it);
             if (!base) continue;
             const uint8_t *rec = base + run_off<FF>(a.H, r0, r);
             const uint8_t *rec_up = base + run_off<FF>(a.H, r0, r1) + run_off<FF>(a.H, r0, r);
             const int nb = FF::rec_blocks(a.H, r);
             const int k0 = r * FF::QK;
-            {   // gate record, then up record: one record's registers live at a time
-                typename FF::W w;
-                FF::load_s(w, rec, nb, lane);
-#pragma unroll
-                for (int i = 0; i < NT; ++i) {
-                    if (i < U.nt) {
-                        const Act x = act_view(xq(tok[i]), a.H);
-                        int is[FF::NSUB];
-                        FF::isums(w, x, k0, nb, is);
-                        ag[i] = __fadd_rn(ag[i], FF::combine(w, x, k0, nb, is));
-                    }
-                }
-            }
-            {
-                typename FF::W w;
-                FF::load_s(w, rec_up, nb, lane);
-                free_item(it);
-#pragma unroll
-                for (int i = 0; i < NT; ++i) {
-                    if (i < U.nt) {
-                        const Act x = act_view(xq(tok[i]), a.H);
-                        int is[FF::NSUB];
-                        FF::isums(w, x, k0, nb, is);
-                        au[i] = __fadd_rn(au[i], FF::combine(w, x, k0, nb, is));
-                    }
-                }
-            }
+            rec_dot<FF, NT>((uint32_t)(rec - sm), nb, k0, a.H, o.xq, (uint32_t)a.xrec, tok, U.nt, lane, ag);
+            rec_dot<FF, NT>((uint32_t)(rec_up - sm), nb, k0, a.H, o.xq, (uint32_t)a.xrec, tok, U.nt, lane, au);
+            free_item(it);
         }
         item += U.nitems;
         // NT <= 4: two reduction buffers alternate; NT = 16: one buffer, and
@@ -484,8 +567,8 @@ struct LayerKernel {
 
     // expert key of B unit j: MAXP for the shared expert, else its unique index
     __device__ int b_key(int j) {
-        if (j < m->nA + m->n_sb) return MAXP;
-        return (j - m->nA - m->n_sb) / m->tilesH;
+        if (j < p.nA + p.n_sb) return MAXP;
+        return div_tiles(j - p.nA - p.n_sb, p.tilesH, p.invH);
     }
     __device__ int key_pairs(int key) { return key == MAXP ? a.T : uoff()[key + 1] - uoff()[key]; }
 
@@ -515,7 +598,7 @@ struct LayerKernel {
         int *keys = m->kkey;
         if (threadIdx.x == 0) {
             int nk = 0, used = 0, n = n0;
-            for (; n < nend; ++n) {
+            for (; n < nend && n - n0 < 64; ++n) {
                 const int key = b_key(b_unit(n));
                 bool seen = false;
                 for (int q = 0; q < nk; ++q) seen |= keys[q] == key;
@@ -589,30 +672,24 @@ struct LayerKernel {
     __device__ void run_B_warp(const Unit &U, int item, int slot0) {
         const int Irows = U.kind == 2 ? a.Is : a.I;
         float ao[NT];
+        int sidx[NT];   // hq slots of the unit's pairs
 #pragma unroll
-        for (int i = 0; i < NT; ++i) ao[i] = 0.f;
+        for (int i = 0; i < NT; ++i) { ao[i] = 0.f; sidx[i] = slot0 + i; }
         for (int q = 0; q < U.nitems; ++q) {
             int r0, r1;
             item_recs(U, q, r0, r1);
             const uint8_t *base = wait_item(item + q);
             if (!base) continue;
-            for (int r = r0; r < r1; ++r) {
-                typename FF::W wd;
-                const int nb = FF::rec_blocks(Irows, r);
-                FF::load_s(wd, base + run_off<FF>(Irows, r0, r), nb, lane);
-                if (r == r1 - 1) free_item(item + q);   // the item's last record is in registers
-                const int k0 = r * FF::QK;
-#pragma unroll
-                for (int i = 0; i < NT; ++i) {
-                    if (i < U.nt) {
-                        const Act h = act_view(hq(slot0 + i), Irows);
-                        int is[FF::NSUB];
-                        FF::isums(wd, h, k0, nb, is);
-                        ao[i] = __fadd_rn(ao[i], FF::combine(wd, h, k0, nb, is));
-                    }
-                }
-            }
+            for (int r = r0; r < r1; ++r)
+                rec_dot<FF, NT>((uint32_t)(base - sm + run_off<FF>(Irows, r0, r)), FF::rec_blocks(Irows, r), r * FF::QK,
+                                Irows, o.hq, (uint32_t)a.hrec, sidx, U.nt, lane, ao);
+            free_item(item + q, (uint32_t)(r1 - r0));
         }
+        store_o(U, ao);
+    }
+
+    // o rows of a B unit (its expert's down bias added), as tagged words
+    __device__ void store_o(const Unit &U, const float *ao) {
         const int row = U.rt * 32 + lane;
         const float bd = (U.kind == 3 && U.ex->b_down) ? U.ex->b_down[row] : 0.f;
 #pragma unroll
@@ -628,23 +705,122 @@ struct LayerKernel {
         }
     }
 
+    // One record of a B unit into partial slot t: o-row partial sums of that
+    // record alone (fresh accumulators, so the later in-order sum of the
+    // slots equals the unit's sequential sum bit for bit).
+    template <class FF>
+    __device__ void run_B_record(const Unit &U, int it0, int slot0, int r, int t) {
+        const int Irows = U.kind == 2 ? a.Is : a.I;
+        const int q = r >> a.lgrb, r0 = q << a.lgrb;
+        float pt[NT];
+        int sidx[NT];
+#pragma unroll
+        for (int i = 0; i < NT; ++i) { pt[i] = 0.f; sidx[i] = slot0 + i; }
+        const uint8_t *base = wait_item(it0 + q);
+        if (base) {
+            rec_dot<FF, NT>((uint32_t)(base - sm + run_off<FF>(Irows, r0, r)), FF::rec_blocks(Irows, r), r * FF::QK,
+                            Irows, o.hq, (uint32_t)a.hrec, sidx, U.nt, lane, pt);
+            free_item(it0 + q);
+        }
+        float *part = reinterpret_cast<float *>(sm + o.red);
+#pragma unroll
+        for (int i = 0; i < NT; ++i) part[(t * NT + i) * 32 + lane] = pt[i];
+    }
+
+    // warp 0: the unit table of B units [n, n1) (at most 64)
+    __device__ void b_table(int n, int n1) {
+        int nr[2], ni[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int k = lane + 32 * h, q = n + k;
+            nr[h] = ni[h] = 0;
+            if (q < n1) {
+                const int j = b_unit(q), key = b_key(j);
+                nr[h] = key == MAXP ? FS::nrec(a.Is) : F::nrec(a.I);
+                ni[h] = (nr[h] + (1 << a.lgrb) - 1) >> a.lgrb;
+                m->bt_j[k] = j;
+                m->bt_slot[k] = key_slot(key);
+            }
+        }
+        int carry_r = 0, carry_i = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            int sr = nr[h], si = ni[h];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int vr = __shfl_up_sync(0xFFFFFFFFu, sr, off), vi = __shfl_up_sync(0xFFFFFFFFu, si, off);
+                if (lane >= off) { sr += vr; si += vi; }
+            }
+            const int k = lane + 32 * h;
+            m->bt_rec[k] = carry_r + sr - nr[h];
+            m->bt_it[k] = carry_i + si - ni[h];
+            carry_r += __shfl_sync(0xFFFFFFFFu, sr, 31);
+            carry_i += __shfl_sync(0xFFFFFFFFu, si, 31);
+        }
+        // entries past the batch hold the totals (their counts are zero)
+        if (lane == 0) { m->bt_rec[64] = carry_r; m->bt_it[64] = carry_i; }
+    }
+
+    // B units of one hq batch.  Groups of whole units with at most LW records
+    // in all (or one unit) are spread record by record over the warps: each
+    // record's partial sums go to a slot of the reduction buffer, then one
+    // warp per unit adds its slots in record order and writes the o rows.  A
+    // unit with more records than the buffer has slots runs on one warp.
+    __device__ void run_B_batch(int n, int n1, int &item) {
+        constexpr int CAP = NT <= 4 ? 32 : 16;   // record slots in the reduction buffer
+        if (warp == 0) b_table(n, n1);
+        cbar();
+        const int nu = n1 - n;
+        const int *brec = m->bt_rec;
+        for (int k = 0; k < nu;) {
+            int ke = k + 1;
+            while (ke < nu && brec[ke + 1] - brec[k] <= LW) ++ke;
+            const int recs = brec[ke] - brec[k];
+            if (recs > CAP) {   // one long unit: the warp-per-unit path
+                if (warp == 0) {
+                    Unit U;
+                    unit_of(m->bt_j[k], U);
+                    if (std::is_same<F, FS>::value || U.kind == 3) run_B_warp<F>(U, item + m->bt_it[k], m->bt_slot[k]);
+                    else run_B_warp<FS>(U, item + m->bt_it[k], m->bt_slot[k]);
+                }
+                k = ke;
+                continue;
+            }
+            for (int t = warp; t < recs; t += LW) {
+                int kk = k;
+                while (brec[kk + 1] - brec[k] <= t) ++kk;
+                Unit U;
+                unit_of(m->bt_j[kk], U);
+                const int r = t - (brec[kk] - brec[k]);
+                if (std::is_same<F, FS>::value || U.kind == 3) run_B_record<F>(U, item + m->bt_it[kk], m->bt_slot[kk], r, t);
+                else run_B_record<FS>(U, item + m->bt_it[kk], m->bt_slot[kk], r, t);
+            }
+            cbar();
+            const float *part = reinterpret_cast<const float *>(sm + o.red);
+            for (int kk = k + warp; kk < ke; kk += LW) {
+                Unit U;
+                unit_of(m->bt_j[kk], U);
+                float ao[NT];
+#pragma unroll
+                for (int i = 0; i < NT; ++i) ao[i] = 0.f;
+                for (int s = brec[kk] - brec[k]; s < brec[kk + 1] - brec[k]; ++s) {
+#pragma unroll
+                    for (int i = 0; i < NT; ++i) ao[i] = __fadd_rn(ao[i], part[(s * NT + i) * 32 + lane]);
+                }
+                store_o(U, ao);
+            }
+            cbar();   // the next group reuses the slots
+            k = ke;
+        }
+        item += m->bt_it[nu];
+    }
+
     __device__ void run_B_phase(int &item) {
-        const int nend = m->nb;
+        const int nend = p.nb;
         int n = 0;
         while (n < nend) {
             const int n1 = load_hq_batch(n, nend);
-            int it = item;
-            for (int q = n; q < n1; ++q) {
-                Unit U;
-                unit_of(b_unit(q), U);
-                if (((q - n) & (LW - 1)) == warp) {
-                    const int slot = key_slot(U.kind == 2 ? MAXP : U.u);
-                    if (std::is_same<F, FS>::value || U.kind == 3) run_B_warp<F>(U, it, slot);
-                    else run_B_warp<FS>(U, it, slot);
-                }
-                it += U.nitems;
-            }
-            item = it;
+            run_B_batch(n, n1, item);
             cbar();   // the next batch overwrites hq
             n = n1;
         }
@@ -665,19 +841,17 @@ struct LayerKernel {
         for (int t = 0; t < a.T; ++t) {
             float y = 0.f;
             for (int s0 = 0; s0 < a.k; s0 += 8) {
+                const int n = min(8, a.k - s0);
                 tword w[8];
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const int s = s0 + jj, p = t * a.k + s;
-                    w[jj] = (s < a.k && pu()[p] >= 0) ? ld_tag(a.o_r + (size_t)p * a.H + row) : 0ull;
+                for (int jj = 0; jj < 8; ++jj) {   // slots not owned here count as present
+                    const int p = t * a.k + s0 + jj;
+                    if (jj < n) w[jj] = pu()[p] >= 0 ? ld_tag(a.o_r + (size_t)p * a.H + row) : ((tword)ep << 32);
                 }
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) {
-                    const int s = s0 + jj, p = t * a.k + s;
-                    if (s < a.k && pu()[p] >= 0) {
-                        const float v = tag_value(wait_tag(a.o_r + (size_t)p * a.H + row, w[jj]));
-                        y += wts()[p] * v;
-                    }
+                    const int p = t * a.k + s0 + jj;
+                    if (jj < n && pu()[p] >= 0) y += wts()[p] * tag_value(wait_tag(a.o_r + (size_t)p * a.H + row, w[jj]));
                 }
             }
             if (a.shared) {
@@ -711,7 +885,9 @@ struct LayerKernel {
         const int chunks = (a.H + 255) / 256;
         for (int w = warp; w < a.T * chunks; w += LW) {
             const int t = w / chunks, ch = w - t * chunks;
-            quant_chunk256<false>(a.x + (size_t)t * a.H, a.H, 256 * ch, xq(t), lane);
+            float v[8];
+            const bool act = quant_load8<false>(a.x + (size_t)t * a.H, a.H, 256 * ch, lane, v);
+            quant_store8(v, act, a.H, 256 * ch, xq(t), lane);
         }
     }
 
@@ -839,13 +1015,10 @@ struct LayerKernel {
         }
         int myid = 0;
         uint32_t mykey = 0u;
-        if (K > 0) {
-#pragma unroll
-            for (int s = 0; s < K; ++s) topk_round<JN>(key, s, myid, mykey);
-        } else {
+        // rounds as a loop, not unrolled: this code runs once per launch and
+        // fetching it cold costs more than the loop's own instructions
 #pragma unroll 1
-            for (int s = 0; s < a.k; ++s) topk_round<JN>(key, s, myid, mykey);
-        }
+        for (int s = 0; s < (K > 0 ? K : a.k); ++s) topk_round<JN>(key, s, myid, mykey);
         if (lane < a.k) out[lane] = myid;
         return fkey_value(mykey);
     }
@@ -859,21 +1032,21 @@ struct LayerKernel {
         }
     }
 
+    // every logit: each consumer thread loads its words (up to 8) at once and
+    // re-reads the ones not yet published, in rounds
     __device__ void topk_and_group() {
         float *lgs = reinterpret_cast<float *>(sm + o.lg);
         const int TE = a.T * a.E;
-        for (int i0 = threadIdx.x; i0 < TE; i0 += 4 * LW * 32) {
-            tword w[4];
+        for (int i0 = threadIdx.x; i0 < TE; i0 += 8 * LW * 32) {
+            const int n = min(8, (TE - i0 + LW * 32 - 1) / (LW * 32));
+            tword w[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int i = i0 + q * LW * 32;
-                w[q] = i < TE ? ld_tag(a.logits + i) : 0ull;
-            }
+            for (int q = 0; q < 8; ++q)
+                if (q < n) w[q] = ld_tag(a.logits + i0 + q * LW * 32);
+            wait_tags(a.logits + i0, LW * 32, n, w);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int i = i0 + q * LW * 32;
-                if (i < TE) lgs[i] = tag_value(wait_tag(a.logits + i, w[q]));
-            }
+            for (int q = 0; q < 8; ++q)
+                if (q < n) lgs[i0 + q * LW * 32] = tag_value(w[q]);
         }
         cbar();
         for (int t = warp; t < a.T; t += LW) {
@@ -1013,6 +1186,7 @@ struct LayerKernel {
         }
         cbar();
         plan();
+        load_plan();
     }
 
     // unit counts and this block's B range: every block's A bytes follow from
@@ -1036,11 +1210,11 @@ struct LayerKernel {
                 m->n_rb = m->U * m->tilesH;
                 m->nB = m->n_sb + m->n_rb;
                 m->bsnake = 1;
-                int p = 0;
-                while (snake_unit(p, c, G) < m->nA) ++p;
-                m->bp0 = p;
+                int pass = 0;
+                while (snake_unit(pass, c, G) < m->nA) ++pass;
+                m->bp0 = pass;
                 int n = 0;
-                while (snake_unit(p + n, c, G) < m->nA + m->nB) ++n;
+                while (snake_unit(pass + n, c, G) < m->nA + m->nB) ++n;
                 m->nb = n;
             }
             cbar();
@@ -1063,8 +1237,8 @@ struct LayerKernel {
         cbar();
         u64 my_a = 0;
         if (tid < G) {
-            for (int p = 0; p * G < m->nA; ++p) {
-                const int j = snake_unit(p, tid, G);
+            for (int pass = 0; pass * G < m->nA; ++pass) {
+                const int j = snake_unit(pass, tid, G);
                 if (j < m->n_sa) my_a += sa;
                 else if (j < m->nA) my_a += ra;
             }
@@ -1096,7 +1270,7 @@ struct LayerKernel {
 
     // the n-th B unit of this block (global unit index)
     __device__ int b_unit(int n) {
-        return m->bsnake ? snake_unit(m->bp0 + n, c, G) : m->nA + m->jb0 + n;
+        return p.bsnake ? snake_unit(p.bp0 + n, c, G) : p.nA + p.jb0 + n;
     }
 
     // first B unit whose byte midpoint is >= X (B list: shared units of sb
@@ -1127,6 +1301,7 @@ struct LayerKernel {
             m->nA = m->n_sa;
         }
         __syncthreads();
+        load_plan();   // the shared-expert A units; the rest follows the routing plan
         if (warp == LW) {
             producer();
         } else {
@@ -1150,20 +1325,23 @@ struct LayerKernel {
                 if (rbytes) bulk_g2s(sm + o.router, (const uint8_t *)a.w_router + (size_t)e0 * rowb, rbytes, fixed_bar());
                 if (tb) bulk_g2s(sm + o.table, a.experts, tb, fixed_bar());
             }
-            for (int p = 0; !m->abort; ++p) {
-                const int j = snake_unit(p, c, G);
-                if (p * G >= m->n_sa) break;
-                if (j < m->n_sa && !issue_unit(R, j)) break;
+            for (int pass = 0; !m->abort; ++pass) {
+                const int j = snake_unit(pass, c, G);
+                if (pass * G >= p.n_sa) break;
+                if (j < p.n_sa && !issue_unit(R, j)) break;
             }
         }
+        if (lane == 0 && a.shared) m->shx = *a.shared;   // for units after the handoff
         __syncthreads();   // routing handoff: the plan is ready
+        shp = &m->shx;
+        load_plan();
         if (lane == 0 && !m->abort) {
-            for (int p = 0;; ++p) {
-                const int j = snake_unit(p, c, G);
-                if (p * G >= m->nA) break;
-                if (j >= m->n_sa && j < m->nA && !issue_unit(R, j)) break;
+            for (int pass = 0;; ++pass) {
+                const int j = snake_unit(pass, c, G);
+                if (pass * G >= p.nA) break;
+                if (j >= p.n_sa && j < p.nA && !issue_unit(R, j)) break;
             }
-            for (int n = 0; n < m->nb && !m->abort; ++n)
+            for (int n = 0; n < p.nb && !m->abort; ++n)
                 if (!issue_unit(R, b_unit(n))) break;
         }
         // drain: no copy may still be writing this block's shared memory at exit
@@ -1187,10 +1365,10 @@ struct LayerKernel {
         router_logits();
         // shared-expert gate/up while the other blocks publish their logits
         int item = 0, rbuf = 0;
-        for (int p = 0;; ++p) {
-            const int j = snake_unit(p, c, G);
-            if (p * G >= m->n_sa) break;
-            if (j < m->n_sa) {
+        for (int pass = 0;; ++pass) {
+            const int j = snake_unit(pass, c, G);
+            if (pass * G >= p.n_sa) break;
+            if (j < p.n_sa) {
                 Unit U;
                 unit_of(j, U);
                 run_A<FS>(U, item, rbuf);
@@ -1199,10 +1377,10 @@ struct LayerKernel {
         topk_and_group();
         bar_handoff();
         gating_weights();
-        for (int p = 0;; ++p) {
-            const int j = snake_unit(p, c, G);
-            if (p * G >= m->nA) break;
-            if (j >= m->n_sa && j < m->nA) {
+        for (int pass = 0;; ++pass) {
+            const int j = snake_unit(pass, c, G);
+            if (pass * G >= p.nA) break;
+            if (j >= p.n_sa && j < p.nA) {
                 Unit U;
                 unit_of(j, U);
                 run_A<F>(U, item, rbuf);
@@ -1215,7 +1393,10 @@ struct LayerKernel {
     }
 
     // the handoff barrier pairs with the producer's __syncthreads
-    __device__ void bar_handoff() { __syncthreads(); }
+    __device__ void bar_handoff() {
+        __syncthreads();
+        shp = &m->shx;
+    }
 
     // block 0 advances the epoch once it is done: every block read it before
     // publishing its logits, which block 0 has consumed; the next launch reads
@@ -1227,8 +1408,7 @@ struct LayerKernel {
 
 template <class F, class FS, int NT>
 __global__ void __launch_bounds__(LT, 1) layer_kernel(const __grid_constant__ LayerArgs a) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    LayerKernel<F, FS, NT> K(a, smem);
+    LayerKernel<F, FS, NT> K(a, moe_smem);
     K.run();
 }
 

@@ -48,13 +48,11 @@ static uint32_t max_item(int q, int H, int I) {
     const uint32_t a = 2 * max_rec(q, H), b = max_rec(q, I);
     return a > b ? a : b;
 }
-// records per ring item: as many as keep an item within a quarter of the ring
-// (fewer, larger copies land sooner), between 1 and 8
-static int recs_per_item(size_t ring, uint32_t rec_bytes) {
-    size_t r = ring / 4 / rec_bytes;
-    if (r < 1) r = 1;
-    if (r > 8) r = 8;
-    return (int)r;
+// log2 of the records per ring item: the largest power of two (1 to 8) that
+// keeps an item within a quarter of the ring (fewer, larger copies land sooner)
+static int lg_recs_per_item(size_t ring, uint32_t rec_bytes) {
+    const size_t r = ring / 4 / rec_bytes;
+    return r >= 8 ? 3 : (r >= 4 ? 2 : (r >= 2 ? 1 : 0));
 }
 
 cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStream_t s) {
@@ -113,8 +111,8 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
             if (sa > pa) pa = sa;
             if (sb > pb) pb = sb;
         }
-        a.ra = recs_per_item(ring, pa);
-        a.rb = recs_per_item(ring, pb);
+        a.lgra = lg_recs_per_item(ring, pa);
+        a.lgrb = lg_recs_per_item(ring, pb);
     }
     o.ring = take(ring);
     o.bars = take((2 * kNBAR + 1) * 8);

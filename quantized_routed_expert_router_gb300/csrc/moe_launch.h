@@ -68,7 +68,7 @@ struct LayerArgs {
     int table_in_smem;
     int hq_slots;                   // q8 records of requantised h the block can hold
     uint32_t ring_bytes;
-    int ra, rb;                     // records per ring item: A (gate + up runs), B (down run)
+    int lgra, lgrb;                 // log2 of the records per ring item: A (gate + up runs), B (down run)
     size_t xrec, hrec;
     Smem sm;
 };
