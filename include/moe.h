@@ -247,10 +247,13 @@ moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, con
                                   cudaStream_t stream);
 
 /*
- * The whole layer in one launch: quantise (moe_quantize_q8K's rule), route
- * (moe_route's fixed-order logits, top-k and gating) and the routed + shared
- * expert FFN (moe_expert_ffn's arithmetic), for decode where the three steps
- * sit back to back.  One persistent block per SM: every block quantises x and
+ * The whole layer: quantise (moe_quantize_q8K's rule), route (moe_route's
+ * fixed-order logits, top-k and gating) and the routed + shared expert FFN
+ * (moe_expert_ffn's arithmetic), for decode where the three steps sit back to
+ * back.  For T <= 4 this is one launch, described below; larger batches run
+ * the three calls in turn (their kernels keep more warps per SM busy once
+ * every weight record is dotted with many tokens), inside the same workspace.
+ * One persistent block per SM: every block quantises x and
  * computes the logits of its own router rows, every block reads all logits,
  * selects the same top-k and streams its share of the chosen experts' packed
  * weights with TMA bulk copies into a shared-memory ring.  Logits, h and the
@@ -266,7 +269,7 @@ moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, con
  *   ws          : device workspace of moe_layer_workspace_bytes() bytes,
  *                 zero-filled before its first use and after any call that set
  *                 MOE_DEV_TIMEOUT; completed calls leave it ready for the next
- *   flags       : MOE_LAYER_OVERLAP_PREVIOUS lets this launch start while the
+ *   flags       : (T <= 4) MOE_LAYER_OVERLAP_PREVIOUS lets this launch start while the
  *                 previous kernel in the stream is still running (programmatic
  *                 dependent launch): before that kernel has finished, the call
  *                 reads only weights, router and expert tables, so none of those

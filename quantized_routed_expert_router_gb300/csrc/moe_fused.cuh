@@ -1444,7 +1444,7 @@ template <class F, class FS>
 cudaError_t launch_layer_nt(const LayerArgs &a, int G, size_t smem, bool pdl, cudaStream_t s) {
     if (a.NT == 1) return launch_layer_t<F, FS, 1>(a, G, smem, pdl, s);
     if (a.NT == 4) return launch_layer_t<F, FS, 4>(a, G, smem, pdl, s);
-    return launch_layer_t<F, FS, 16>(a, G, smem, pdl, s);
+    return cudaErrorNotSupported;
 }
 
 }  // namespace moe

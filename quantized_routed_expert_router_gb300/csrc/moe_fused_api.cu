@@ -70,7 +70,7 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
     a.xrec = q8_row_bytes(a.H);
     const int Imax = a.Is > a.I ? a.Is : a.I;
     a.hrec = q8_row_bytes(Imax);
-    a.NT = a.T <= 1 ? 1 : (a.T <= 4 ? 4 : 16);
+    a.NT = a.T <= 1 ? 1 : 4;   // batches above 4 tokens never reach the fused kernel
     const size_t red_bytes = (size_t)(a.NT <= 4 ? 2 : 1) * kLW * 2 * a.NT * 32 * 4;
 
     Smem o;
@@ -150,10 +150,35 @@ bool fmt_ok(int q) { return q == MOE_Q8_0 || q == MOE_Q4_K || q == MOE_Q2_K || q
 bool cols_ok(int q, int cols) { return cols > 0 && (q == MOE_MXFP4 ? cols % 32 == 0 : cols % 256 == 0); }
 }  // namespace
 
+// Batches above this size take the three separate kernels: every record is
+// then dotted with many tokens, and the persistent kernel's eight consumer
+// warps per SM run out of latency hiding where the separate kernels, with
+// several blocks per SM, do not.
+constexpr int kFusedMaxTokens = 4;
+
+// workspace of the separate-kernel route for larger batches: the FFN
+// workspace first (its status word is the layer's), then the router's, the
+// q8 activations, ids and weights
+struct SplitWs {
+    size_t ffn, route, xq, ids, w, total;
+};
+SplitWs split_ws_layout(int T, int k, const moe_pool *pool, const moe_pool *shared) {
+    auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    SplitWs s;
+    s.ffn = 0;
+    s.route = al(moe_ffn_workspace_bytes(T, k, pool, shared));
+    s.xq = al(s.route + moe_route_workspace_bytes(T, pool->E, pool->H));
+    s.ids = al(s.xq + (size_t)T * q8_row_bytes(pool->H));
+    s.w = al(s.ids + 4 * (size_t)T * k);
+    s.total = al(s.w + 4 * (size_t)T * k);
+    return s;
+}
+
 extern "C" {
 
 size_t moe_layer_workspace_bytes(int T, int k, const moe_pool *pool, const moe_pool *shared) {
     if (T < 1 || k < 1 || !pool) return 0;
+    if (T > kFusedMaxTokens) return split_ws_layout(T, k, pool, shared).total;
     return layer_ws_layout(T, k, pool->H, pool->I, shared ? shared->I : 0, pool->E).total;
 }
 
@@ -178,6 +203,20 @@ moe_status moe_layer_forward(const float *hidden, int T, const void *w_router, m
     if (T == 0) return MOE_OK;
     if (!hidden || !w_router || !y || !al16p(hidden) || !al16p(w_router) || !al16p(y)) return MOE_ERR_INVALID_ARG;
     if (xq_out && !al16p(xq_out)) return MOE_ERR_INVALID_ARG;
+    if (T > kFusedMaxTokens) {   // the three kernels back to back, through their own entry points
+        const SplitWs S = split_ws_layout(T, k, pool, shared);
+        if (!ws || ws_bytes < S.total || !al16p(ws)) return MOE_ERR_WORKSPACE;
+        char *w = (char *)ws;
+        void *xq = xq_out ? xq_out : (void *)(w + S.xq);
+        int32_t *ids = ids_out ? ids_out : (int32_t *)(w + S.ids);
+        float *wts = weights_out ? weights_out : (float *)(w + S.w);
+        moe_status st = moe_quantize_q8K(hidden, T, H, xq, stream);
+        if (st == MOE_OK)
+            st = moe_route(hidden, xq, T, H, w_router, rtype, E, router_bias, k, gating, renormalize, ids, wts,
+                           logits_out, w + S.route, S.xq - S.route, stream);
+        if (st == MOE_OK) st = moe_expert_ffn(xq, T, ids, wts, k, pool, shared, y, w + S.ffn, S.route, stream);
+        return st;
+    }
     const LayerWs L = layer_ws_layout(T, k, H, I, shared ? shared->I : 0, E);
     if (!ws || ws_bytes < L.total || !al16p(ws)) return MOE_ERR_WORKSPACE;
     char *w = (char *)ws;
