@@ -347,7 +347,7 @@ def main():
         import oracle
         n = 0
         t0 = time.perf_counter()
-        while time.perf_counter() - t0 < 10.0 and n < 40:
+        while time.perf_counter() - t0 < 10.0 and n < 100000:
             oracle.layer_forward(host_sample[n % len(host_sample)])
             n += 1
         dt = time.perf_counter() - t0
