@@ -1354,15 +1354,23 @@ struct LayerKernel {
     __device__ void consumer() {
         pdl_wait();
         if (threadIdx.x == 0) m->ep = ld_relaxed_u32(a.epoch) + 1u;
-        quantise_x();
+        // an fp32 router needs only x: its logits go out first and x is
+        // quantised while the other blocks publish theirs; a Q8_0 router dots
+        // the quantised x
+        const bool xq_first = a.rtype == MOE_Q8_0;
+        if (xq_first) quantise_x();
         cbar();
         ep = m->ep;
+        router_logits();
+        if (!xq_first) {
+            quantise_x();
+            cbar();
+        }
         if (c == 0 && a.xq_out) {
             const int n16 = (int)(a.xrec / 16);
             for (int i = threadIdx.x; i < a.T * n16; i += LW * 32)
                 reinterpret_cast<uint4 *>(a.xq_out)[i] = reinterpret_cast<const uint4 *>(sm + o.xq)[i];
         }
-        router_logits();
         // shared-expert gate/up while the other blocks publish their logits
         int item = 0, rbuf = 0;
         for (int pass = 0;; ++pass) {
