@@ -614,6 +614,7 @@ struct LayerKernel {
             m->bend = n;
         }
         cbar();
+        if (warp == 0) b_table(n0, m->bend);   // the batch's unit table, while h is still arriving
         const int nk = m->nkeys;
         const bool ok = !m->abort;
         // tasks (key, pair, 256-chunk), flattened; a warp loads the h of up to
@@ -727,7 +728,8 @@ struct LayerKernel {
         for (int i = 0; i < NT; ++i) part[(t * NT + i) * 32 + lane] = pt[i];
     }
 
-    // warp 0: the unit table of B units [n, n1) (at most 64)
+    // warp 0: the unit table of B units [n, n1) (at most 64), built while the
+    // batch's h is requantised
     __device__ void b_table(int n, int n1) {
         int nr[2], ni[2];
 #pragma unroll
@@ -768,9 +770,7 @@ struct LayerKernel {
     // unit with more records than the buffer has slots runs on one warp.
     __device__ void run_B_batch(int n, int n1, int &item) {
         constexpr int CAP = NT <= 4 ? 32 : 16;   // record slots in the reduction buffer
-        if (warp == 0) b_table(n, n1);
-        cbar();
-        const int nu = n1 - n;
+        const int nu = n1 - n;   // the unit table was built by load_hq_batch
         const int *brec = m->bt_rec;
         for (int k = 0; k < nu;) {
             int ke = k + 1;
