@@ -21,6 +21,10 @@ SMALL = {
                                                           shared_I=512), 2),
     "a22b q4_K T=16 zipf": (synth.shrink(synth.CONFIGS["a22b"], H=1024, I=768, E=24, k=4), 16),
     "a22b q4_K T=1": (synth.shrink(synth.CONFIGS["a22b"], H=1024, I=768, E=24, k=4), 1),
+    # 1024 experts: the expert table stays in global memory and the top-k
+    # holds 32 keys per lane; k = 32 is the largest selection
+    "E1024 k32 T=1": (synth.shrink(synth.CONFIGS["a3b"], H=512, I=256, E=1024, k=32, shared_I=256), 1),
+    "E1024 k32 T=3": (synth.shrink(synth.CONFIGS["a3b"], H=512, I=256, E=1024, k=32, shared_I=256), 3),
 }
 
 
@@ -38,7 +42,7 @@ def test_fused_layer_parity(name, flags):
     dl.forward()                                   # three-call path
     torch.cuda.synchronize()
     y3 = np_(dl.y).copy()
-    for rep in range(3):                           # tickets must rearm between calls
+    for rep in range(3):                           # the epoch advances between calls
         dl.y.fill_(float("nan"))
         dl.ids.fill_(-1)
         dl.forward_fused(flags=flags)
