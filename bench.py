@@ -199,7 +199,7 @@ def run_reference(args, cfg, L, rank, world):
               f"single-threaded scalar C oracle")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32 dots + fp64 combine",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",   # exact int32 dots, fp64 scale combine
             "data": "synthetic",
             "config": {"workload": workload_name(cfg, L, args.tokens), "tokens": args.tokens, "layers": L},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
@@ -359,8 +359,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "int8 dp4a dots + fp32 combine (q4_K/q8_K)" if cfg.qtype == synth.Q4_K
-            else "int8 dp4a dots + fp32 combine",
+            "dtype": "int8",   # int8 x int8 -> int32 sub-block dots; fp32 scale combine
             "data": "synthetic",
             "config": {"workload": workload_name(cfg, L, T), "tokens": T, "layers": L,
                        "l2": f"inputs larger than L2: {step_bytes / 1e6:.0f} MB of distinct weights touched "
