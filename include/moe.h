@@ -269,6 +269,8 @@ moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, con
  *   ws          : device workspace of moe_layer_workspace_bytes() bytes,
  *                 zero-filled before its first use and after any call that set
  *                 MOE_DEV_TIMEOUT; completed calls leave it ready for the next
+ *                 call with the same T (zero-fill it again before a call with
+ *                 another T: the layouts differ)
  *   flags       : (T <= 4) MOE_LAYER_OVERLAP_PREVIOUS lets this launch start while the
  *                 previous kernel in the stream is still running (programmatic
  *                 dependent launch): before that kernel has finished, the call
