@@ -159,35 +159,6 @@ static __device__ __noinline__ tword wait_tag_slow(const tword *p, uint32_t ep, 
         }
     }
 }
-// words[q] (q < n) were loaded from base + q * stride; re-read, in rounds that
-// issue every load still needed at once, until all carry epoch ep (bounded;
-// on timeout the values are not used).  One round trip per round rather than
-// one per word.
-template <int N>
-static __device__ __noinline__ void wait_tags_slow(const tword *base, int stride, int n, tword *words, uint32_t ep,
-                                                  Misc *m, unsigned *status) {
-    tword w[N];
-#pragma unroll
-    for (int q = 0; q < N; ++q) w[q] = q < n ? words[q] : ((tword)ep << 32);
-    const long long t0 = clock64();
-    for (;;) {
-#pragma unroll
-        for (int q = 0; q < N; ++q)
-            if (tag_of(w[q]) != ep) w[q] = ld_tag(base + (size_t)q * stride);
-        bool all = true;
-#pragma unroll
-        for (int q = 0; q < N; ++q) all &= tag_of(w[q]) == ep;
-        if (all) break;
-        if (m->abort || clock64() - t0 > WAIT_CYCLES) {
-            fail_dev(m, status);
-            break;
-        }
-    }
-#pragma unroll
-    for (int q = 0; q < N; ++q)
-        if (q < n) words[q] = w[q];
-}
-
 // ring item i: its slot tag set by the producer (a consumer ahead of the
 // producer sleeps between polls: a tight loop of shared-memory loads by eight
 // warps slows the producer), then its full barrier; false on abort or timeout
@@ -327,14 +298,6 @@ struct LayerKernel {
     // w, already loaded from p, if it carries this launch's epoch, else p re-read
     __device__ __forceinline__ tword wait_tag(const tword *p, tword w) {
         return tag_of(w) == ep ? w : wait_tag_slow(p, ep, m, a.status);
-    }
-    // n <= 8 words loaded from base + q * stride: all of them with this epoch
-    __device__ __forceinline__ void wait_tags(const tword *base, int stride, int n, tword *w) {
-        bool all = true;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            if (q < n) all &= tag_of(w[q]) == ep;
-        if (!all) wait_tags_slow<8>(base, stride, n, w, ep, m, a.status);
     }
 
     // ------------------------------------------------------------ units
@@ -568,8 +531,8 @@ struct LayerKernel {
     // pairs fit the hq buffer together (at most 64 experts, chosen by thread
     // 0): requantise those experts' h into hq.  Returns the end of the run.
     // lane's 8 h values (8 lane .. 8 lane + 7 of the 256-chunk at c0) from
-    // tagged words: four 16-byte loads, then a bounded re-read of any word
-    // that does not carry this launch's epoch yet; false past the row
+    // tagged words: four 16-byte loads, repeated (bounded) until all carry
+    // this launch's epoch; false past the row
     __device__ bool load8_tagged(const tword *x, int n, int c0, float v[8]) {
         const int e0 = c0 + 8 * lane;
         if (e0 >= n || m->abort) {
@@ -580,8 +543,28 @@ struct LayerKernel {
         tword w[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) ld_tag2(x + e0 + 2 * i, w[2 * i], w[2 * i + 1]);
+        // one warp store wrote all eight words, so they turn up together:
+        // re-read all of them per round (one round trip), not word by word
+        bool all = true;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = tag_value(wait_tag(x + e0 + i, w[i]));
+        for (int i = 0; i < 8; ++i) all &= tag_of(w[i]) == ep;
+        if (!all) {
+            const long long t0 = clock64();
+            for (;;) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) ld_tag2(x + e0 + 2 * i, w[2 * i], w[2 * i + 1]);
+                all = true;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) all &= tag_of(w[i]) == ep;
+                if (all) break;
+                if (m->abort || clock64() - t0 > WAIT_CYCLES) {
+                    fail();
+                    break;
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = tag_value(w[i]);
         return true;
     }
 
@@ -827,7 +810,7 @@ struct LayerKernel {
     }
 
     // y rows of one 32-row tile: slots in slot order, shared expert last.
-    // A token's tagged o words are all loaded before any is waited on.
+    // A token's tagged o words are loaded, and re-read, together.
     __device__ void write_y(int rt) {
         const int row = rt * 32 + lane;
         for (int t = 0; t < a.T; ++t) {
@@ -840,10 +823,32 @@ struct LayerKernel {
                     const int p = t * a.k + s0 + jj;
                     if (jj < n) w[jj] = pu()[p] >= 0 ? ld_tag(a.o_r + (size_t)p * a.H + row) : ((tword)ep << 32);
                 }
+                {   // re-read every missing word per round: one round trip each
+                    bool all = true;
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj)
+                        if (jj < n) all &= tag_of(w[jj]) == ep;
+                    const long long t0 = clock64();
+                    while (!all) {
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const int p = t * a.k + s0 + jj;
+                            if (jj < n && tag_of(w[jj]) != ep) w[jj] = ld_tag(a.o_r + (size_t)p * a.H + row);
+                        }
+                        all = true;
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj)
+                            if (jj < n) all &= tag_of(w[jj]) == ep;
+                        if (!all && (m->abort || clock64() - t0 > WAIT_CYCLES)) {
+                            fail();
+                            break;
+                        }
+                    }
+                }
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) {
                     const int p = t * a.k + s0 + jj;
-                    if (jj < n && pu()[p] >= 0) y += wts()[p] * tag_value(wait_tag(a.o_r + (size_t)p * a.H + row, w[jj]));
+                    if (jj < n && pu()[p] >= 0) y += wts()[p] * tag_value(w[jj]);
                 }
             }
             if (a.shared) {
@@ -1035,7 +1040,26 @@ struct LayerKernel {
 #pragma unroll
             for (int q = 0; q < 8; ++q)
                 if (q < n) w[q] = ld_tag(a.logits + i0 + q * LW * 32);
-            wait_tags(a.logits + i0, LW * 32, n, w);
+            {   // re-read every missing word per round: one round trip each
+                bool all = true;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q < n) all &= tag_of(w[q]) == ep;
+                const long long t0 = clock64();
+                while (!all) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        if (q < n && tag_of(w[q]) != ep) w[q] = ld_tag(a.logits + i0 + q * LW * 32);
+                    all = true;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        if (q < n) all &= tag_of(w[q]) == ep;
+                    if (!all && (m->abort || clock64() - t0 > WAIT_CYCLES)) {
+                        fail();
+                        break;
+                    }
+                }
+            }
 #pragma unroll
             for (int q = 0; q < 8; ++q)
                 if (q < n) lgs[i0 + q * LW * 32] = tag_value(w[q]);
