@@ -9,26 +9,31 @@
 //     dependent launch), the producer bulk-copies input-independent bytes
 //     into shared memory: this block's router rows, the expert pointer table
 //     and the first shared-expert gate/up records.
-//  2. After griddepcontrol.wait every block quantises x itself (no exchange),
-//     computes logits for its router rows in the fixed summation order and
-//     publishes them; while the other blocks finish, it runs its share of the
-//     shared expert's gate/up.
+//  2. After griddepcontrol.wait every block computes the logits of its
+//     router rows in the fixed summation order and publishes them, then
+//     quantises x itself (a Q8_0 router dots the quantised x, so it
+//     quantises first); while the other blocks finish, it runs its share of
+//     the shared expert's gate/up.
 //  3. Every block reads every logit and selects the same top-k, groups the
 //     (token, slot) pairs by expert and derives the same work plan:
 //       A units = (expert, 32-row tile of I): gate + up records,
 //       B units = (expert, 32-row tile of H): down records.
-//     A units are dealt out in a snake over blocks; B units are contiguous
-//     ranges sized so every block streams about the same number of bytes.
-//  4. The producer streams each unit's records (TMA bulk copies, complete_tx
-//     mbarriers) through a byte ring; consumer warp r % 8 takes record r of a
-//     unit, so every sum has a fixed order whatever the batch.
-//  5. An A unit ends with h = silu(g) * u rows in global scratch; a B unit's
-//     block first requantises its expert's h locally, and the unit ends with
-//     o rows; row tile rt of y is written by block rt % G, which sums the
-//     slots of each token in slot order (shared expert last).
+//     A units are dealt out in a snake over blocks; for one token the B
+//     units continue the snake, otherwise they are contiguous ranges sized
+//     so every block streams about the same number of bytes.
+//  4. The producer streams the units' records (TMA bulk copies, complete_tx
+//     mbarriers) through a byte ring, up to eight records per copy; consumer
+//     warp r % 8 takes record r of an A unit, and a batch's B records are
+//     spread over the warps with per-record partial sums added in record
+//     order, so every sum has a fixed order whatever the batch.
+//  5. An A unit ends with h = silu(g) * u rows in global scratch; a B
+//     batch's block first requantises its experts' h locally, and each B
+//     unit ends with o rows; row tile rt of y is written by block rt % G,
+//     which sums the slots of each token in slot order (shared expert last).
 //  Exchanges between blocks (logits, h, o) carry no separate flag: every
 //  value is stored with this launch's epoch in one 8-byte word, and a reader
-//  polls the words it needs until they carry the epoch.  An 8-byte aligned
+//  polls the words it needs, re-reading all the missing ones each round,
+//  until they carry the epoch.  An 8-byte aligned
 //  access is single-copy atomic, so a word with the right epoch holds the
 //  right value and no fence is needed on either side.  The epoch is a counter
 //  in the workspace: read after the dependency wait, written back (+1) by
