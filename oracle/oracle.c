@@ -42,6 +42,12 @@
  *
  * Where the pages leave a step open, the readings are the ones listed in the
  * design notes (R1..R14 there); each is marked READING below.
+ *
+ * Parity unpinned: the byte layout of the GGUF-style blocks.  The pages print
+ * no worked example of any block; the block decoders are pinned to hand-
+ * derived closed forms on the stated fields (and to the generator's encoders),
+ * which fixes this file's reading of the layouts but not its byte-for-byte
+ * agreement with real GGUF files.
  */
 #include <stdint.h>
 #include <stddef.h>
