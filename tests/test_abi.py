@@ -74,3 +74,38 @@ def test_argument_errors_return_before_launch():
     assert L.moe_expert_ffn(1 << 20, 0, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, 1 << 20, None, 0, s) == 0
     assert L.moe_debug_row_dots(None, moe.Q4_K, 32, 256, 0, None, None, s) == INVALID
     assert moe.status_str(3).startswith("workspace")
+
+
+def test_layer_call_sizes_and_argument_errors():
+    """The layer call's workspace follows its batch-size dispatch, and its
+    argument and workspace checks return before anything is launched."""
+    L = moe.lib()
+    INVALID, UNSUP, WS = 1, 2, 3
+    s = ctypes.c_void_p(0)
+    pool = moe._Pool(moe.Q4_K, 2048, 512, 256, 1 << 20)
+    shared = moe._Pool(moe.Q4_K, 2048, 512, 1, 1 << 21)
+    wsz = {T: L.moe_layer_workspace_bytes(T, 8, ctypes.byref(pool), ctypes.byref(shared)) for T in (1, 4, 5, 16)}
+    assert all(v > 0 for v in wsz.values())
+    assert wsz[1] < wsz[4]                       # one persistent launch: tagged words per pair
+    assert wsz[5] < wsz[16]                      # separate kernels: their own workspaces
+    assert L.moe_layer_workspace_bytes(0, 8, ctypes.byref(pool), None) == 0
+    P = 1 << 20
+
+    def call(T=1, k=8, pool_=pool, shared_=shared, rtype=moe.F32, ws=None, ws_bytes=0, hidden=P):
+        return L.moe_layer_forward(hidden, T, P, rtype, None, k, 0, 1, ctypes.byref(pool_),
+                                   ctypes.byref(shared_) if shared_ is not None else None, P,
+                                   None, None, None, None, ws, ws_bytes, 0, s)
+
+    assert call(T=17) == INVALID                  # above the token limit
+    assert call(k=300) == INVALID                 # k > E
+    assert call(rtype=moe.Q4_K) == UNSUP          # routers are F32 or Q8_0
+    assert call(hidden=None) == INVALID
+    assert call(hidden=P + 4) == INVALID          # hidden must be 16-byte aligned
+    assert call(T=0) == 0                         # no tokens: nothing to do
+    for T in (1, 4, 16):                          # both dispatch paths check the workspace first
+        assert call(T=T) == WS
+        assert call(T=T, ws=P, ws_bytes=wsz[T] - 1) == WS
+    odd = moe._Pool(moe.Q4_K, 2048, 512, 1, 1 << 21)
+    odd_shared_h = moe._Pool(moe.Q4_K, 1024, 512, 1, 1 << 21)
+    assert call(shared_=odd_shared_h) == INVALID  # the shared expert must match H
+    assert call(shared_=odd) == WS
