@@ -92,3 +92,34 @@ def test_fused_back_to_back_layers_with_overlap():
         for L, dl in zip(layers, dls):
             assert moe.moe_read_device_status(dl.ws_layer) == 0
             assert_y_close(np_(dl.y), oracle.layer_forward(L)["y"], f"layer {L.layer}")
+
+
+def test_fused_stack_replayed_from_a_cuda_graph():
+    """The benchmark's launch configuration: a stack of distinct layers captured
+    once in a CUDA graph with the overlap flag, replayed many times.  Every
+    replay must give the oracle's y (the per-launch epoch advances on the
+    device, so stale words of an earlier replay are never taken), and y must
+    be written afresh by each replay."""
+    cfg = synth.shrink(synth.CONFIGS["a3b"], H=1024, I=512, E=32, k=4, shared_I=256)
+    layers = [synth.make_layer(cfg, l, T=1) for l in range(5)]
+    refs = [oracle.layer_forward(L)["y"] for L in layers]
+    dls = [DeviceLayer(L, "cuda") for L in layers]
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for dl in dls:   # one eager pass first (kernel attributes are set on first use)
+            dl.forward_fused(flags=moe.LAYER_OVERLAP_PREVIOUS, outputs=False)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for dl in dls:
+            dl.forward_fused(flags=moe.LAYER_OVERLAP_PREVIOUS, outputs=False)
+    for rep in range(4):
+        for dl in dls:
+            dl.y.fill_(float("nan"))
+        torch.cuda.synchronize()
+        for _ in range(rep + 1):
+            g.replay()
+        torch.cuda.synchronize()
+        for L, dl, ref in zip(layers, dls, refs):
+            assert moe.moe_read_device_status(dl.ws_layer) == 0
+            assert_y_close(np_(dl.y), ref, f"replay {rep}, layer {L.layer}")
