@@ -429,3 +429,22 @@ def test_synth_is_deterministic():
     assert np.array_equal(a, b) and not np.array_equal(a, c)
     x = synth.normal(0, 1, 1.0, 1, 100000)
     assert abs(x.mean()) < 0.02 and abs(x.std() - 1) < 0.02
+
+
+def test_zipf_router_bias_skews_selection():
+    """The 16-token batch of the 235B-A22B-style stack adds b_e = -1.1 ln(rank_e)
+    to the logits, ranks a seeded permutation of 1..E per layer: tokens then
+    share experts far more often than with the plain router."""
+    cfg = synth.CONFIGS["a22b"]
+    b0, b0_again, b1 = synth.zipf_bias(cfg, 0), synth.zipf_bias(cfg, 0), synth.zipf_bias(cfg, 1)
+    expect = np.sort((-1.1 * np.log(np.arange(1, cfg.E + 1, dtype=np.float64))).astype(np.float32))
+    assert np.array_equal(np.sort(b0), expect)
+    assert np.array_equal(b0, b0_again) and not np.array_equal(b0, b1)
+    small = synth.shrink(cfg, H=512)
+    L = synth.make_layer(small, 0, T=16, zipf=False, with_experts=False)
+    W = np.asarray(L.router, np.float32).reshape(small.E, small.H)
+    plain = oracle.router_logits(W, L.x)
+    skewed = oracle.router_logits(W, L.x, bias=synth.zipf_bias(small, 0))
+    u_plain = len(np.unique(oracle.topk(plain, small.k)[0]))
+    u_skewed = len(np.unique(oracle.topk(skewed, small.k)[0]))
+    assert u_skewed < u_plain, (u_skewed, u_plain)
