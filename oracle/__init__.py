@@ -23,7 +23,7 @@ _SO = os.path.join(_HERE, "_oracle.so")
 _lock = threading.Lock()
 _h = None
 
-F32, Q8_0, Q4_K, Q2_K, MXFP4 = 0, 1, 2, 3, 4
+F32, Q8_0, Q4_K, Q2_K, MXFP4, Q6_K, Q3_K = 0, 1, 2, 3, 4, 5, 6
 SOFTMAX, SIGMOID = 0, 1
 _P = ctypes.c_void_p
 
@@ -155,8 +155,8 @@ def topk(logits, k, gating=SOFTMAX, renorm=True):
 
 
 def row_isums(qtype, row, cols, xq_row):
-    qk = {Q4_K: 256, Q2_K: 256, Q8_0: 32, MXFP4: 32}[qtype]
-    nsub = {Q4_K: 8, Q2_K: 16, Q8_0: 1, MXFP4: 1}[qtype]
+    qk = {Q4_K: 256, Q2_K: 256, Q6_K: 256, Q3_K: 256, Q8_0: 32, MXFP4: 32}[qtype]
+    nsub = {Q4_K: 8, Q2_K: 16, Q6_K: 16, Q3_K: 16, Q8_0: 1, MXFP4: 1}[qtype]
     out = np.zeros(cols // qk * nsub, np.int32)
     row, xq_row = _c(row, np.uint8), _c(xq_row, np.int8)
     if _lib().oracle_row_isums(qtype, row.ctypes.data, cols, xq_row.ctypes.data, out.ctypes.data):

@@ -20,12 +20,20 @@ Formats (GGUF-style blocks; element value in terms of the stored fields):
   MXFP4: {u8 e; u8 qs[16]}                 w = 2^(e-127) * E2M1(code)
          code of element j < 16 is the low nibble of qs[j], of j+16 the high
          nibble; bit 3 is the sign.
+  Q6_K : {u8 ql[128]; u8 qh[64]; i8 sc[16]; f16 d}
+         w = d sc_j (c - 32) over 16 sub-blocks of 16, c a 6-bit code: for
+         element 128n+32s+l its low nibble is nibble s//2 of ql[64n+32(s%2)+l]
+         and its top 2 bits are bits 2s..2s+1 of qh[32n+l].
+  Q3_K : {u8 hmask[32]; u8 qs[64]; u8 sc[12]; f16 d}
+         w = d (s_j - 32) c over 16 sub-blocks of 16, c = (2 bits at 2s of
+         qs[32n+l]) - 4 * (1 - bit 4n+s of hmask[l]); 6-bit s_j: nibble j//8
+         of byte j%8 plus 2 high bits at 2(j//4) of byte 8 + j%4.
 """
 from __future__ import annotations
 
 import numpy as np
 
-F32, Q8_0, Q4_K, Q2_K, MXFP4 = 0, 1, 2, 3, 4
+F32, Q8_0, Q4_K, Q2_K, MXFP4, Q6_K, Q3_K = 0, 1, 2, 3, 4, 5, 6
 _E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], np.float64)
 
 
@@ -77,6 +85,32 @@ def dequant(qtype: int, blocks: np.ndarray, cols: int) -> np.ndarray:
         mag = _E2M1[code & 7]
         val = np.where(code & 8, -mag, mag)
         return (scale[..., None] * val).reshape(rows, cols)
+    if qtype == Q6_K:
+        b = blocks.reshape(rows, cols // 256, 210).astype(np.int64)
+        ql = b[..., 0:128].reshape(rows, -1, 2, 2, 32)                  # [.., n, s%2, l]
+        qh = b[..., 128:192].reshape(rows, -1, 2, 1, 32)                # [.., n, 1, l]
+        lo = np.concatenate([ql & 15, ql >> 4], axis=-2)                # [.., n, s, l], s = 2*(nibble) + s%2
+        hi = (qh >> (2 * np.arange(4).reshape(4, 1))) & 3
+        code = (lo | (hi << 4)) - 32
+        sc = blocks.reshape(rows, cols // 256, 210)[..., 192:208].view(np.int8).astype(np.float64)
+        d = _f16(blocks.reshape(rows, cols // 256, 210)[..., 208:210])
+        w = d[..., None, None] * sc[..., None] * code.reshape(rows, -1, 16, 16).astype(np.float64)
+        return w.reshape(rows, cols)
+    if qtype == Q3_K:
+        raw = blocks.reshape(rows, cols // 256, 110)
+        b = raw.astype(np.int64)
+        hm = b[..., 0:32].reshape(rows, -1, 1, 1, 32)
+        qs = b[..., 32:96].reshape(rows, -1, 2, 1, 32)
+        s = np.arange(4).reshape(1, 4, 1)
+        n = np.arange(2).reshape(2, 1, 1)
+        code = ((qs >> (2 * s)) & 3) - 4 * (1 - ((hm >> (4 * n + s)) & 1))   # [.., n, s, l]
+        s12 = b[..., 96:108]
+        low = np.concatenate([s12[..., 0:8] & 15, s12[..., 0:8] >> 4], axis=-1)
+        high = np.stack([(s12[..., 8:12] >> (2 * g)) & 3 for g in range(4)], axis=-2).reshape(rows, -1, 16)
+        scale = ((low | (high << 4)) - 32).astype(np.float64)
+        d = _f16(raw[..., 108:110])
+        w = d[..., None, None] * scale[..., None] * code.reshape(rows, -1, 16, 16).astype(np.float64)
+        return w.reshape(rows, cols)
     raise ValueError(qtype)
 
 

@@ -35,13 +35,20 @@
  *      Q4_K : d_x * (d * sum_j sc_j isum_j - dmin * sum_j m_j bsum_j), 32-sub-blocks
  *      Q2_K : the same over 16-sub-blocks
  *      MXFP4: 2^(e-128) * d_x * sum v_i q_i, v = 2 * E2M1 value
+ *      Q6_K : d_x * d * sum_j sc_j isum_j, signed 6-bit codes q - 32, int8
+ *             scales, 16-sub-blocks (the model table's Q6_K matmuls on q8_K)
+ *      Q3_K : d_x * d * sum_j (s_j - 32) isum_j, 3-bit codes in [-4, 3],
+ *             6-bit scales, 16-sub-blocks (the q3_K expert tensors of the
+ *             streaming-lane notes)
  *    g and u (+ biases) give h = silu(g) * u (fp64, rounded to fp32 where the
  *    method stores it), h is requantised with the activation rule above, the
  *    down projection (+ bias) gives o, and y = sum over slots in slot order
  *    of w * o, plus the shared expert with weight 1, added last.
  *
- * Where the pages leave a step open, the readings are the ones listed in the
- * design notes (R1..R14 there); each is marked READING below.
+ * Where the pages leave a step open, the step states the reading it takes and
+ * is marked READING below: the router's summation order, the symmetric
+ * activation scale, and the layouts of the Q6_K and Q3_K blocks (the pages
+ * name those two formats but print no field list).
  *
  * Parity unpinned: the byte layout of the GGUF-style blocks.  The pages print
  * no worked example of any block; the block decoders are pinned to hand-
@@ -54,7 +61,7 @@
 #include <string.h>
 #include <math.h>
 
-enum { OQ_F32 = 0, OQ_Q8_0 = 1, OQ_Q4_K = 2, OQ_Q2_K = 3, OQ_MXFP4 = 4 };
+enum { OQ_F32 = 0, OQ_Q8_0 = 1, OQ_Q4_K = 2, OQ_Q2_K = 3, OQ_MXFP4 = 4, OQ_Q6_K = 5, OQ_Q3_K = 6 };
 
 /* ------------------------------------------------------------ decoding */
 
@@ -106,19 +113,57 @@ static int mxfp4_v(const uint8_t *blk, int j) {
     return (c & 8) ? -mag[c & 7] : mag[c & 7];
 }
 
+/* READING: Q6_K and Q3_K follow the public GGUF block layouts.
+ * Q6_K super-block {ql[128], qh[64], i8 sc[16], f16 d}: signed code of
+ * element i.  With i = 128n + 32s + l, the low nibble sits in byte
+ * 64n + l + 32*(s odd) of ql (upper nibble when s >= 2) and the top two bits
+ * in bits 2s, 2s+1 of qh[32n + l]; the stored 6-bit value is offset by 32. */
+static int q6k_code(const uint8_t *blk, int i) {
+    int n = i / 128, s = (i % 128) / 32, l = i % 32;
+    int lo = blk[64 * n + 32 * (s % 2) + l];
+    lo = (s >= 2) ? (lo >> 4) : (lo & 15);
+    int hi = (blk[128 + 32 * n + l] >> (2 * s)) & 3;
+    return (lo | (hi << 4)) - 32;
+}
+
+static int q6k_scale(const uint8_t *blk, int j) { return (int8_t)blk[192 + j]; }
+
+/* Q3_K super-block {hmask[32], qs[64], sc[12], f16 d}: signed code of
+ * element i = 128n + 32s + l is the 2-bit field at bits 2s, 2s+1 of
+ * qs[32n + l], minus 4 unless bit 4n + s of hmask[l] is set. */
+static int q3k_code(const uint8_t *blk, int i) {
+    int n = i / 128, s = (i % 128) / 32, l = i % 32;
+    int lo = (blk[32 + 32 * n + l] >> (2 * s)) & 3;
+    int set = (blk[l] >> (4 * n + s)) & 1;
+    return set ? lo : lo - 4;
+}
+
+/* Q3_K scale of sub-block j (0..15): 4 low bits from the nibbles of bytes
+ * 0..7 (j < 8: low nibble of byte j; else high nibble of byte j - 8), 2 high
+ * bits from byte 8 + j%4 at bit 2*(j/4); the 6-bit value is offset by 32. */
+static int q3k_scale(const uint8_t *blk, int j) {
+    const uint8_t *s = blk + 96;
+    int low = (j < 8) ? (s[j] & 15) : (s[j - 8] >> 4);
+    int high = (s[8 + j % 4] >> (2 * (j / 4))) & 3;
+    return (low | (high << 4)) - 32;
+}
+
 int oracle_block_elems(int qt) {
-    return qt == OQ_Q4_K || qt == OQ_Q2_K ? 256 : (qt == OQ_F32 ? 1 : 32);
+    switch (qt) { case OQ_F32: return 1; case OQ_Q8_0: case OQ_MXFP4: return 32;
+                  case OQ_Q4_K: case OQ_Q2_K: case OQ_Q6_K: case OQ_Q3_K: return 256; }
+    return -1;
 }
 int oracle_block_bytes(int qt) {
     switch (qt) { case OQ_F32: return 4; case OQ_Q8_0: return 34; case OQ_Q4_K: return 144;
-                  case OQ_Q2_K: return 84; case OQ_MXFP4: return 17; }
+                  case OQ_Q2_K: return 84; case OQ_MXFP4: return 17; case OQ_Q6_K: return 210;
+                  case OQ_Q3_K: return 110; }
     return -1;
 }
 
 /* sub-blocks per weight block, for the integer-dot listing */
 int oracle_subblocks(int qt) {
-    switch (qt) { case OQ_Q4_K: return 8; case OQ_Q2_K: return 16; case OQ_Q8_0: return 1;
-                  case OQ_MXFP4: return 1; }
+    switch (qt) { case OQ_Q4_K: return 8; case OQ_Q2_K: case OQ_Q6_K: case OQ_Q3_K: return 16;
+                  case OQ_Q8_0: return 1; case OQ_MXFP4: return 1; }
     return -1;
 }
 
@@ -150,6 +195,12 @@ int oracle_dequant_row(int qt, const uint8_t *row, int cols, double *out) {
         } else if (qt == OQ_MXFP4) {
             double s = ldexp(1.0, (int)blk[0] - 128);
             for (int i = 0; i < 32; ++i) o[i] = s * mxfp4_v(blk, i);
+        } else if (qt == OQ_Q6_K) {
+            double d = oracle_f16(rd16(blk + 208));
+            for (int i = 0; i < 256; ++i) o[i] = d * q6k_scale(blk, i / 16) * q6k_code(blk, i);
+        } else if (qt == OQ_Q3_K) {
+            double d = oracle_f16(rd16(blk + 108));
+            for (int i = 0; i < 256; ++i) o[i] = d * q3k_scale(blk, i / 16) * q3k_code(blk, i);
         }
     }
     return 0;
@@ -200,7 +251,7 @@ static float butterfly32(float v[32]) {
     return v[0];
 }
 
-/* fp32 router, canonical order (READING R1) */
+/* fp32 router, canonical order (READING: the order stated in the header) */
 int oracle_router_f32(const float *W, int E, int H, const float *x, int T,
                       const float *bias, float *logits) {
     if (H % 4) return -1;
@@ -325,6 +376,8 @@ int oracle_row_isums(int qt, const uint8_t *row, int cols, const int8_t *xq, int
         int q[256];
         if (qt == OQ_Q4_K) q4k_codes(blk, q);
         else if (qt == OQ_Q2_K) q2k_codes(blk, q);
+        else if (qt == OQ_Q6_K) for (int i = 0; i < 256; ++i) q[i] = q6k_code(blk, i);
+        else if (qt == OQ_Q3_K) for (int i = 0; i < 256; ++i) q[i] = q3k_code(blk, i);
         else if (qt == OQ_Q8_0) for (int i = 0; i < 32; ++i) q[i] = (int8_t)blk[2 + i];
         else for (int i = 0; i < 32; ++i) q[i] = mxfp4_v(blk, i);
         for (int j = 0; j < nsub; ++j) {
@@ -362,6 +415,13 @@ double oracle_row_dot(int qt, const uint8_t *row, int cols, const float *xd, con
                 M += (long long)m * (bs[2 * j] + bs[2 * j + 1]);
             }
             term = dx * ((double)oracle_f16(rd16(blk)) * (double)P - (double)oracle_f16(rd16(blk + 2)) * (double)M);
+        } else if (qt == OQ_Q6_K || qt == OQ_Q3_K) {
+            /* no min term: the codes are signed */
+            long long P = 0;
+            for (int j = 0; j < 16; ++j)
+                P += (long long)(qt == OQ_Q6_K ? q6k_scale(blk, j) : q3k_scale(blk, j)) * is[j];
+            double d = oracle_f16(rd16(blk + (qt == OQ_Q6_K ? 208 : 108)));
+            term = dx * (d * (double)P);
         } else {
             long long P = 0, M = 0;
             for (int j = 0; j < 16; ++j) {

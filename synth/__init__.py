@@ -27,11 +27,14 @@ _SO = os.path.join(_HERE, "_synth.so")
 _lock = threading.Lock()
 _lib_handle = None
 
-# qtype codes (the same numbering as the library's public enum)
-F32, Q8_0, Q4_K, Q2_K, MXFP4 = 0, 1, 2, 3, 4
-QTYPE_NAMES = {F32: "f32", Q8_0: "q8_0", Q4_K: "q4_K", Q2_K: "q2_K", MXFP4: "mxfp4"}
+# qtype codes: 0..4 are the library's public enum; Q6_K and Q3_K are generated
+# for the CPU oracle only (the library rejects those codes)
+F32, Q8_0, Q4_K, Q2_K, MXFP4, Q6_K, Q3_K = 0, 1, 2, 3, 4, 5, 6
+QTYPE_NAMES = {F32: "f32", Q8_0: "q8_0", Q4_K: "q4_K", Q2_K: "q2_K", MXFP4: "mxfp4", Q6_K: "q6_K",
+               Q3_K: "q3_K"}
 # (elements per block, bytes per block)
-BLOCK = {F32: (1, 4), Q8_0: (32, 34), Q4_K: (256, 144), Q2_K: (256, 84), MXFP4: (32, 17)}
+BLOCK = {F32: (1, 4), Q8_0: (32, 34), Q4_K: (256, 144), Q2_K: (256, 84), MXFP4: (32, 17),
+         Q6_K: (256, 210), Q3_K: (256, 110)}
 
 
 def build(force: bool = False) -> str:

@@ -3,7 +3,7 @@
  *
  * This module is input generation only.  It draws normal variates from
  * counter-keyed splitmix64 streams and encodes weight matrices into the
- * GGUF-style block layouts (Q8_0, Q4_K, Q2_K, MXFP4) that both the CUDA
+ * GGUF-style block layouts (Q8_0, Q4_K, Q2_K, MXFP4, Q6_K, Q3_K) that the CUDA
  * library and the CPU oracle consume.  It computes nothing of the MoE path
  * itself (no dots, no routing, no activation quantisation).
  *
@@ -24,6 +24,13 @@
  *   Q2_K   : the same with 16-sub-blocks, 2-bit q, 4-bit sc/m, /3 and /15.
  *   MXFP4  : e = ceil(log2(max|w|/6)), stored e+127; each w/2^e rounded to the
  *            nearest E2M1 value, ties to the even code.
+ *   Q6_K   : per 16-sub-block step = max|w|/31; d = max step/127 (f16);
+ *            int8 sc = rint(step/d); q = clamp(rint(w/(d*sc)), -32, 31),
+ *            stored as q + 32 (low nibble in ql, top 2 bits in qh).
+ *   Q3_K   : per 16-sub-block step = max|w|/4; d = max step/31 (f16);
+ *            6-bit s = rint(step/d) + 32 (scale s - 32);
+ *            q = clamp(rint(w/(d*(s-32))), -4, 3), stored as 2 low bits of
+ *            q + 4 in qs and a high-mask bit set when q >= 0.
  */
 #include <stdint.h>
 #include <stddef.h>
@@ -273,8 +280,89 @@ static void enc_mxfp4(const float *w, int64_t cols, uint8_t *out) {
     }
 }
 
-/* qtype codes shared with the library's public enum */
-enum { Q_F32 = 0, Q_Q8_0 = 1, Q_Q4_K = 2, Q_Q2_K = 3, Q_MXFP4 = 4 };
+/* Q6_K: {u8 ql[128]; u8 qh[64]; i8 sc[16]; f16 d} = 210 B per 256 weights.
+ * Element 128n + 32s + l (half n, quarter s, lane l) keeps its low nibble in
+ * ql[64n + 32(s&1) + l] (low nibble for s < 2, high for s >= 2) and its top
+ * two bits at bits 2s..2s+1 of qh[32n + l]; sub-block j = i/16 uses sc[j]. */
+static void enc_q6_k(const float *w, int64_t cols, uint8_t *out) {
+    for (int64_t b = 0; b < cols / 256; ++b) {
+        const float *x = w + 256 * b;
+        uint8_t *blk = out + 210 * b;
+        float step[16], smx = 0.f;
+        for (int j = 0; j < 16; ++j) {
+            float amax = 0.f;
+            for (int i = 0; i < 16; ++i) { float a = fabsf(x[16 * j + i]); if (a > amax) amax = a; }
+            step[j] = amax / 31.f;
+            if (step[j] > smx) smx = step[j];
+        }
+        uint16_t dh = f32_to_f16(smx / 127.f);
+        float d = f16_value(dh);
+        int sc[16], q[256];
+        for (int j = 0; j < 16; ++j) sc[j] = d > 0.f ? clampi((int)rintf(step[j] / d), 0, 127) : 0;
+        for (int i = 0; i < 256; ++i) {
+            float st = d * (float)sc[i / 16];
+            q[i] = (st > 0.f ? clampi((int)rintf(x[i] / st), -32, 31) : 0) + 32;
+        }
+        uint8_t *ql = blk, *qh = blk + 128;
+        memset(blk, 0, 192);
+        for (int n = 0; n < 2; ++n)
+            for (int s = 0; s < 4; ++s)
+                for (int l = 0; l < 32; ++l) {
+                    int v = q[128 * n + 32 * s + l];
+                    ql[64 * n + 32 * (s & 1) + l] |= (uint8_t)((v & 15) << (s < 2 ? 0 : 4));
+                    qh[32 * n + l] |= (uint8_t)((v >> 4) << (2 * s));
+                }
+        for (int j = 0; j < 16; ++j) blk[192 + j] = (uint8_t)(int8_t)sc[j];
+        memcpy(blk + 208, &dh, 2);
+    }
+}
+
+/* Q3_K: {u8 hmask[32]; u8 qs[64]; u8 sc[12]; f16 d} = 110 B per 256 weights.
+ * Element 128n + 32s + l keeps 2 low bits at bits 2s..2s+1 of qs[32n + l] and
+ * its high bit at bit 4n + s of hmask[l]; value q = low - (high ? 0 : 4).
+ * The 6-bit scale s_j of sub-block j = i/16 keeps its low nibble in sc[j]
+ * (j < 8) or the high nibble of sc[j - 8] (j >= 8), and its top two bits at
+ * bits 2(j/4)..2(j/4)+1 of sc[8 + j%4]. */
+static void enc_q3_k(const float *w, int64_t cols, uint8_t *out) {
+    for (int64_t b = 0; b < cols / 256; ++b) {
+        const float *x = w + 256 * b;
+        uint8_t *blk = out + 110 * b;
+        float step[16], smx = 0.f;
+        for (int j = 0; j < 16; ++j) {
+            float amax = 0.f;
+            for (int i = 0; i < 16; ++i) { float a = fabsf(x[16 * j + i]); if (a > amax) amax = a; }
+            step[j] = amax / 4.f;
+            if (step[j] > smx) smx = step[j];
+        }
+        uint16_t dh = f32_to_f16(smx / 31.f);
+        float d = f16_value(dh);
+        int sc[16], q[256];
+        for (int j = 0; j < 16; ++j) sc[j] = d > 0.f ? clampi((int)rintf(step[j] / d), 0, 31) : 0;
+        for (int i = 0; i < 256; ++i) {
+            float st = d * (float)sc[i / 16];
+            q[i] = st > 0.f ? clampi((int)rintf(x[i] / st), -4, 3) : 0;
+        }
+        uint8_t *hm = blk, *qs = blk + 32, *s6 = blk + 96;
+        memset(blk, 0, 108);
+        for (int n = 0; n < 2; ++n)
+            for (int s = 0; s < 4; ++s)
+                for (int l = 0; l < 32; ++l) {
+                    int v = q[128 * n + 32 * s + l];
+                    qs[32 * n + l] |= (uint8_t)(((v + 4) & 3) << (2 * s));
+                    if (v >= 0) hm[l] |= (uint8_t)(1 << (4 * n + s));
+                }
+        for (int j = 0; j < 16; ++j) {
+            int v = sc[j] + 32;
+            s6[j < 8 ? j : j - 8] |= (uint8_t)((v & 15) << (j < 8 ? 0 : 4));
+            s6[8 + j % 4] |= (uint8_t)((v >> 4) << (2 * (j / 4)));
+        }
+        memcpy(blk + 108, &dh, 2);
+    }
+}
+
+/* qtype codes: 0..4 are the library's public enum; Q6_K and Q3_K are
+ * generated for the CPU oracle (the library does not accept them yet) */
+enum { Q_F32 = 0, Q_Q8_0 = 1, Q_Q4_K = 2, Q_Q2_K = 3, Q_MXFP4 = 4, Q_Q6_K = 5, Q_Q3_K = 6 };
 
 int64_t synth_row_bytes(int qtype, int64_t cols) {
     switch (qtype) {
@@ -283,6 +371,8 @@ int64_t synth_row_bytes(int qtype, int64_t cols) {
         case Q_Q4_K: return cols % 256 ? -1 : cols / 256 * 144;
         case Q_Q2_K: return cols % 256 ? -1 : cols / 256 * 84;
         case Q_MXFP4: return cols % 32 ? -1 : cols / 32 * 17;
+        case Q_Q6_K: return cols % 256 ? -1 : cols / 256 * 210;
+        case Q_Q3_K: return cols % 256 ? -1 : cols / 256 * 110;
     }
     return -1;
 }
@@ -300,6 +390,8 @@ int synth_encode(int qtype, const float *w, int64_t rows, int64_t cols, void *ou
             case Q_Q4_K: enc_q4_k(x, cols, o); break;
             case Q_Q2_K: enc_q2_k(x, cols, o); break;
             case Q_MXFP4: enc_mxfp4(x, cols, o); break;
+            case Q_Q6_K: enc_q6_k(x, cols, o); break;
+            case Q_Q3_K: enc_q3_k(x, cols, o); break;
             default: return -1;
         }
     }

@@ -60,6 +60,31 @@ def pack_mxfp4(e, codes):
     return np.array([e] + [codes[j] | (codes[j + 16] << 4) for j in range(16)], np.uint8)
 
 
+def pack_q6k(d, sc, c):
+    """c: stored 6-bit codes (value c - 32) in element order; sc: 16 int8 scales."""
+    ql, qh = [0] * 128, [0] * 64
+    for i, v in enumerate(c):
+        half, quarter, lane = divmod(i, 128)[0], (i % 128) // 32, i % 32
+        byte = 64 * half + 32 * (quarter % 2) + lane
+        ql[byte] |= (v & 15) << (4 * (quarter // 2))
+        qh[32 * half + lane] |= (v >> 4) << (2 * quarter)
+    return np.array(ql + qh + [v & 255 for v in sc] + f16_bytes(d), np.uint8)
+
+
+def pack_q3k(d, s6, q):
+    """q: signed 3-bit codes in [-4, 3] in element order; s6: 16 stored 6-bit scales."""
+    hm, qs, sc = [0] * 32, [0] * 64, [0] * 12
+    for i, v in enumerate(q):
+        half, quarter, lane = i // 128, (i % 128) // 32, i % 32
+        qs[32 * half + lane] |= ((v + 4) % 4) << (2 * quarter)
+        if v >= 0:
+            hm[lane] |= 1 << (4 * half + quarter)
+    for j, v in enumerate(s6):
+        sc[j % 8] |= (v & 15) << (4 * (j // 8))
+        sc[8 + j % 4] |= (v >> 4) << (2 * (j // 4))
+    return np.array(hm + qs + sc + f16_bytes(d), np.uint8)
+
+
 E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
 
 
@@ -91,6 +116,16 @@ def build_golden(case):
         scale = 2.0 ** (case["e"] - 127)
         vals = [scale * (-E2M1[c & 7] if c & 8 else E2M1[c & 7]) for c in codes]
         return oracle.MXFP4, blk, 32, vals, np.arange(1, 33).astype(np.int8)
+    if qt == "q6_K":
+        c = [i // 4 for i in range(256)]
+        blk = pack_q6k(case["d"], case["sc"], c)
+        vals = [case["d"] * case["sc"][i // 16] * (c[i] - 32) for i in range(256)]
+        return oracle.Q6_K, blk, 256, vals, np.ones(256, np.int8)
+    if qt == "q3_K":
+        q = [(7 * i + i // 128) % 8 - 4 for i in range(256)]
+        blk = pack_q3k(case["d"], case["s6"], q)
+        vals = [case["d"] * (case["s6"][i // 16] - 32) * q[i] for i in range(256)]
+        return oracle.Q3_K, blk, 256, vals, np.ones(256, np.int8)
     raise ValueError(qt)
 
 
@@ -151,6 +186,54 @@ def test_closed_form_single_code(pos):
     assert np.array_equal(oracle.dequant_row(oracle.Q2_K, blk2, 256), want2)
 
 
+# every (half, quarter, lane-group) field of the 256-element K-quant layouts
+POSITIONS = [0, 15, 16, 31, 32, 47, 63, 64, 95, 96, 127, 128, 159, 160, 191, 200, 224, 255]
+
+
+@pytest.mark.parametrize("pos", POSITIONS)
+def test_closed_form_single_code_q6k_q3k(pos):
+    """one non-zero code among zero values lands on exactly its element"""
+    sc = [(-1) ** j * (j + 2) for j in range(16)]
+    c = [32] * 256                      # stored 32 is the value 0
+    c[pos] = 5                          # value -27
+    want = np.zeros(256)
+    want[pos] = 0.5 * sc[pos // 16] * (5 - 32)
+    assert np.array_equal(oracle.dequant_row(oracle.Q6_K, pack_q6k(0.5, sc, c), 256), want)
+    c[pos] = 63                         # value 31: both high bits set
+    want[pos] = 0.5 * sc[pos // 16] * 31
+    assert np.array_equal(oracle.dequant_row(oracle.Q6_K, pack_q6k(0.5, sc, c), 256), want)
+    s6 = [(5 * j + 1) % 64 for j in range(16)]
+    for v in (-4, -1, 1, 3):
+        q = [0] * 256
+        q[pos] = v
+        want = np.zeros(256)
+        want[pos] = 0.25 * (s6[pos // 16] - 32) * v
+        assert np.array_equal(oracle.dequant_row(oracle.Q3_K, pack_q3k(0.25, s6, q), 256), want)
+
+
+def test_q6k_q3k_extreme_codes_and_scales():
+    """int8 scale -128 and 127, 6-bit scale 0 (= -32) and 63 (= 31), codes at both ends"""
+    sc = [-128, 127] * 8
+    c = [0 if (i // 16) % 2 == 0 else 63 for i in range(256)]
+    got = oracle.dequant_row(oracle.Q6_K, pack_q6k(0.125, sc, c), 256)
+    want = np.where((np.arange(256) // 16) % 2 == 0, 0.125 * -128 * -32, 0.125 * 127 * 31)
+    assert np.array_equal(got, want)
+    s6 = [0, 63] * 8
+    q = [-4 if (i // 16) % 2 == 0 else 3 for i in range(256)]
+    got = oracle.dequant_row(oracle.Q3_K, pack_q3k(2.0, s6, q), 256)
+    want = np.where((np.arange(256) // 16) % 2 == 0, 2.0 * -32 * -4, 2.0 * 31 * 3)
+    assert np.array_equal(got, want)
+
+
+def test_q6k_q3k_zero_scale_or_code_give_zero():
+    rng = np.random.default_rng(11)
+    c = rng.integers(0, 64, 256).tolist()
+    assert not oracle.dequant_row(oracle.Q6_K, pack_q6k(0.5, [0] * 16, c), 256).any()
+    q = rng.integers(-4, 4, 256).tolist()
+    assert not oracle.dequant_row(oracle.Q3_K, pack_q3k(0.5, [32] * 16, q), 256).any()
+    assert not oracle.dequant_row(oracle.Q3_K, pack_q3k(0.5, list(range(16)), [0] * 256), 256).any()
+
+
 def test_mxfp4_lattice_table():
     for e in (120, 127, 131):
         blk = pack_mxfp4(e, [c % 16 for c in range(32)])
@@ -160,7 +243,7 @@ def test_mxfp4_lattice_table():
 
 
 @pytest.mark.parametrize("qt,rms_bound", [(synth.Q8_0, 0.01), (synth.Q4_K, 0.12), (synth.Q2_K, 0.45),
-                                          (synth.MXFP4, 0.2)])
+                                          (synth.MXFP4, 0.2), (synth.Q6_K, 0.03), (synth.Q3_K, 0.25)])
 def test_encoder_roundtrip(qt, rms_bound):
     """generator encoder -> oracle decoder reproduces the fp32 weights to quantisation noise"""
     w = synth.normal(7, 123, 0.02, 64, 512)
@@ -173,11 +256,20 @@ def test_encoder_roundtrip(qt, rms_bound):
     if qt == synth.Q8_0:
         d = np.abs(w).reshape(64, -1, 32).max(-1, keepdims=True) / 127
         assert np.all(np.abs(deq - w).reshape(64, -1, 32) <= 0.5 * d * 1.01 + 1e-12)
+    if qt in (synth.Q6_K, synth.Q3_K):
+        # the largest |w| of each 16-sub-block comes back within a bounded number
+        # of steps (step = amax/31 for Q6_K, amax/4 for Q3_K): half a step of
+        # rounding plus the rounding of the sub-block scale; a 3-bit code tops
+        # out at +3, so a positive Q3_K maximum can lose one whole step more
+        top, steps = (31, 0.75) if qt == synth.Q6_K else (4, 1.5)
+        amax = np.abs(w.astype(np.float64)).reshape(64, -1, 16).max(-1)
+        dmax = np.abs(deq).reshape(64, -1, 16).max(-1)
+        assert np.all(np.abs(dmax - amax) <= steps * amax / top + 1e-12)
 
 
 # -------------------------------------------------------------- int dots
 
-@pytest.mark.parametrize("qt", [synth.Q8_0, synth.Q4_K, synth.Q2_K, synth.MXFP4])
+@pytest.mark.parametrize("qt", [synth.Q8_0, synth.Q4_K, synth.Q2_K, synth.MXFP4, synth.Q6_K, synth.Q3_K])
 def test_row_isums_equal_integer_dot_of_codes(qt):
     """random code bytes with unit scales: values are the integer codes themselves"""
     rng = np.random.default_rng(3)
@@ -187,6 +279,12 @@ def test_row_isums_equal_integer_dot_of_codes(qt):
         sub = 32
     elif qt == synth.Q2_K:
         blocks = [pack_q2k(1.0, 0.0, [1] * 16, [0] * 16, rng.integers(0, 4, 256).tolist()) for _ in range(2)]
+        sub = 16
+    elif qt == synth.Q6_K:
+        blocks = [pack_q6k(1.0, [1] * 16, rng.integers(0, 64, 256).tolist()) for _ in range(2)]
+        sub = 16
+    elif qt == synth.Q3_K:
+        blocks = [pack_q3k(1.0, [33] * 16, rng.integers(-4, 4, 256).tolist()) for _ in range(2)]
         sub = 16
     elif qt == synth.Q8_0:
         blocks = [pack_q8_0(1.0, rng.integers(-128, 128, 32).tolist()) for _ in range(16)]
@@ -204,10 +302,10 @@ def test_row_isums_equal_integer_dot_of_codes(qt):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("qt", [synth.Q8_0, synth.Q4_K, synth.Q2_K, synth.MXFP4])
+@pytest.mark.parametrize("qt", [synth.Q8_0, synth.Q4_K, synth.Q2_K, synth.MXFP4, synth.Q6_K, synth.Q3_K])
 @pytest.mark.parametrize("B", [256, 32])
 def test_row_dot_matches_fp64_dequant_matmul(qt, B):
-    if qt in (synth.Q4_K, synth.Q2_K) and B == 32:
+    if qt in (synth.Q4_K, synth.Q2_K, synth.Q6_K, synth.Q3_K) and B == 32:
         pytest.skip("K-quants are paired with 256-blocks of activations")
     H = 1024
     W = synth.matrix(qt, 1, 77, 0.02, 8, H)
@@ -346,6 +444,10 @@ SMALL = {
     "q4_K+shared": synth.shrink(synth.CONFIGS["a3b"], H=512, I=256, E=8, k=3, shared_I=256),
     "mxfp4+bias": synth.shrink(synth.CONFIGS["oss20b"], H=320, I=288, E=5, k=2),
     "q2_K+q8_0shared": synth.shrink(synth.CONFIGS["wide"], H=512, I=256, E=8, k=3, shared_I=256),
+    "q6_K+shared": synth.shrink(synth.CONFIGS["a3b"], H=512, I=256, E=8, k=3, shared_I=256,
+                                qtype=synth.Q6_K, shared_qtype=synth.Q6_K),
+    "q3_K+q8_0shared": synth.shrink(synth.CONFIGS["wide"], H=512, I=256, E=8, k=3, shared_I=256,
+                                    qtype=synth.Q3_K),
 }
 
 
