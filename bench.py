@@ -164,6 +164,49 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+def host_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def time_oracle(layers, threads, steps=None, seconds=None):
+    """The CPU oracle's layer forward on `threads` host threads at once.
+
+    Thread i runs oracle.layer_forward over the seeded layers in turn, starting
+    at layer i, for `steps` layer-steps or until `seconds` have passed.  The
+    oracle's work runs in C behind ctypes, which releases the GIL, so the
+    threads run in parallel; the oracle keeps no global state.  Returns
+    (layer-steps done by all threads, wall seconds)."""
+    import threading
+
+    import oracle
+    done, errors = [0] * threads, []
+    t0 = time.perf_counter()
+
+    def work(i):
+        n = 0
+        try:
+            while (steps is None or n < steps) and (seconds is None or time.perf_counter() - t0 < seconds):
+                oracle.layer_forward(layers[(i + n) % len(layers)])
+                n += 1
+        except Exception as e:  # surfaced after the join
+            errors.append(e)
+        done[i] = n
+
+    pool = [threading.Thread(target=work, args=(i,)) for i in range(threads)]
+    for t in pool:
+        t.start()
+    for t in pool:
+        t.join()
+    dt = time.perf_counter() - t0
+    if errors:
+        raise errors[0]
+    return sum(done), dt
+
+
 def layer_bytes(cfg, dl, moe):
     """Algorithmic HBM bytes of one layer-step: unique chosen experts + shared + router + activations."""
     ids = dl.ids.cpu().numpy()
@@ -182,27 +225,23 @@ def layer_bytes(cfg, dl, moe):
 
 
 def run_reference(args, cfg, L, rank, world):
-    import oracle
     import synth
     if rank != 0:
         return
     nsample = 2
     layers = [synth.make_layer(cfg, l, T=args.tokens, seed=args.seed) for l in range(nsample)]
-    for i in range(args.warmup):
-        oracle.layer_forward(layers[i % nsample])
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        oracle.layer_forward(layers[i % nsample])
-    dt = time.perf_counter() - t0
-    v = args.steps * args.tokens / dt
-    sample = (f"one {cfg.name} layer x {args.tokens} token(s) per step, cycling over {nsample} seeded layers; "
-              f"single-threaded scalar C oracle")
+    C = host_threads()
+    time_oracle(layers, C, steps=args.warmup)
+    n, dt = time_oracle(layers, C, steps=args.steps)
+    v = n * args.tokens / dt
+    sample = (f"one {cfg.name} layer x {args.tokens} token(s) per host thread per step ({C} threads at once), "
+              f"cycling over {nsample} seeded layers; scalar C oracle")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",   # exact int32 dots, fp64 scale combine
             "data": "synthetic",
             "config": {"workload": workload_name(cfg, L, args.tokens), "tokens": args.tokens, "layers": L},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": C, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -239,7 +278,7 @@ def main():
     for l in range(L):
         Lh = synth.make_layer(cfg, l, T=T, seed=rank_seed(args.seed, rank))
         layers.append(DeviceLayer(Lh, dev))
-        if l < 2 and rank == 0 and not args.no_cpu:
+        if l < 2 and world == 1 and not args.no_cpu:
             host_sample.append(Lh)
         del Lh
     # one contiguous input and output buffer for the whole stack, so the
@@ -343,17 +382,16 @@ def main():
     achieved = (step_bytes / L) / (launch_ms / 1e3) / 1e9
     traffic = traffic_record(f"layer_kernel:{cfg.name}:T{T}")
     cpu = None
-    if rank == 0 and not args.no_cpu and host_sample:
-        import oracle
-        n = 0
-        t0 = time.perf_counter()
-        while time.perf_counter() - t0 < 10.0 and n < 100000:
-            oracle.layer_forward(host_sample[n % len(host_sample)])
-            n += 1
-        dt = time.perf_counter() - t0
-        cpu = {"value": n * T / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n} layer-steps of {cfg.name} (T={T}) over {len(host_sample)} seeded layers, "
-                         f"single-threaded scalar C oracle, {dt:.1f} s"}
+    if world == 1 and not args.no_cpu and host_sample:
+        # after every GPU leg, so the host threads disturb no GPU timing
+        n1, dt1 = time_oracle(host_sample, 1, steps=100000, seconds=4.0)
+        C = host_threads()
+        n, dt = time_oracle(host_sample, C, steps=100000, seconds=6.0)
+        cpu = {"value": n * T / dt, "unit": UNIT, "cores": C, "kind": "oracle",
+               "sample": f"{n} layer-steps of {cfg.name} (T={T}) on {C} host threads at once over "
+                         f"{len(host_sample)} seeded layers, scalar C oracle, {dt:.1f} s",
+               "single_thread": {"value": n1 * T / dt1, "cores": 1,
+                                 "sample": f"{n1} layer-steps on one thread, {dt1:.1f} s"}}
     if rank == 0:
         uniq = [b["unique"] for b in bytes_l]
         line = {
