@@ -125,18 +125,20 @@ moe_status moe_pack_weights(const void *blocks, moe_qtype qtype, int rows, int c
 /*
  * Activation quantisation (README "MoE resolve": activations quantised to
  * q8_0/q8_K before integer dots).  x: device fp32 [T][n]; xq: device, T
- * records of moe_q8_row_bytes(n), 16-byte aligned.  Per block of
+ * records of moe_q8_row_bytes(n); both 16-byte aligned.  Per block of
  * B = moe_act_block(n): amax = max|x|, d = amax/127, q = rint(x*(127/amax))
  * (round half to even; IEEE division), d = 0 and q = 0 for an all-zero
  * block; bsum = sums of 16 codes.  T in [0, MOE_MAX_TOKENS*64]; T == 0 is a
  * no-op.
+ * Errors: MOE_ERR_UNSUPPORTED if moe_act_block(n) == 0; MOE_ERR_INVALID_ARG
+ * for T out of range or a NULL or unaligned x or xq.
  */
 moe_status moe_quantize_q8K(const float *x, int T, int n, void *xq, cudaStream_t stream);
 
 /*
  * Router GEMV + top-k + gating (README intro: the router stays resident;
  * model table: softmax and sigmoid-gated routers, top-k of E).
- *   hidden      : device fp32 [T][H]   (read by an F32 router)
+ *   hidden      : device fp32 [T][H], 16-byte aligned (read by an F32 router)
  *   xq          : device q8 records of hidden (moe_quantize_q8K), required
  *                 for a Q8_0 router, ignored (may be NULL) for F32
  *   w_router    : device, F32 [E][H] row-major, or Q8_0 blocks [E][H/32]
@@ -150,7 +152,7 @@ moe_status moe_quantize_q8K(const float *x, int T, int n, void *xq, cudaStream_t
  *                 E (renormalize == 0).  Sigmoid: s = 1/(1+exp(-l)), divided
  *                 by the sum over the chosen k when renormalize != 0.
  *   logits_out  : device fp32 [T][E] out, or NULL
- *   ws          : device workspace of moe_route_workspace_bytes(T, E) bytes,
+ *   ws          : device workspace of moe_route_workspace_bytes(T, E, H) bytes,
  *                 zero-filled before its first use; every completed call
  *                 leaves it ready for the next one
  * Logits are fp32 in one fixed summation order, so ids are reproducible bit
@@ -162,6 +164,10 @@ moe_status moe_quantize_q8K(const float *x, int T, int n, void *xq, cudaStream_t
  * segment, value (d_w*d_x)*isum.
  * Limits: 1 <= k <= min(E, MOE_MAX_K), E <= MOE_MAX_EXPERTS, T <= MOE_MAX_TOKENS,
  * H % 32 == 0.
+ * Errors: MOE_ERR_INVALID_ARG for limits, gating, or a NULL or unaligned
+ * buffer; MOE_ERR_UNSUPPORTED for a router type other than F32/Q8_0 or a Q8_0
+ * router with H % 256 != 0; MOE_ERR_WORKSPACE for a missing, short or
+ * unaligned ws.
  */
 moe_status moe_route(const float *hidden, const void *xq, int T, int H,
                      const void *w_router, moe_qtype rtype, int E, const float *router_bias,
@@ -192,12 +198,13 @@ typedef struct {
  * Routed + shared expert FFN for T tokens (README "MoE resolve": integer
  * dots on q8 activations with per-block rescale; SwiGLU; per-slot weighted
  * sum; shared expert always on).
- *   xq      : device q8 records of the T hidden states (width pool->H)
+ *   xq      : device q8 records of the T hidden states (width pool->H),
+ *             16-byte aligned
  *   ids     : device int32 [T][k]; weights: device fp32 [T][k]
  *   pool    : host pointer to the routed pool (qtype Q8_0, Q4_K, Q2_K or MXFP4)
  *   shared  : host pointer to a pool with E == 1 (weight 1, no biases read),
  *             or NULL
- *   y       : device fp32 [T][H] out, overwritten:
+ *   y       : device fp32 [T][H] out, 16-byte aligned, overwritten:
  *             y[t] = sum over slots s in slot order of w[t][s]*o(ids[t][s])
  *                    + o_shared (added last),
  *             o = W_down . q8(h) + b_down,  h = silu(g) * u,
@@ -215,6 +222,10 @@ typedef struct {
  * between T = 1 and any batch that contains it.
  * Limits: T <= MOE_MAX_TOKENS, k <= MOE_MAX_K, E <= MOE_MAX_EXPERTS;
  * H and I multiples of 32 (of 256 for Q4_K, Q2_K, Q8_0).
+ * Errors: MOE_ERR_INVALID_ARG for limits, a pool with no expert table, an
+ * unknown expert format or a NULL or unaligned buffer; MOE_ERR_UNSUPPORTED
+ * for widths the format cannot hold or a shared pool of another H;
+ * MOE_ERR_WORKSPACE for a missing, short or unaligned ws.
  */
 moe_status moe_expert_ffn(const void *xq, int T, const int32_t *ids, const float *weights, int k,
                           const moe_pool *pool, const moe_pool *shared, float *y,
@@ -266,6 +277,7 @@ moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, con
  *                 (shared: the same format as pool or Q8_0)
  *   y           : device fp32 [T][H] out
  *   ids_out, weights_out, logits_out, xq_out: optional outputs (NULL to skip)
+ *   hidden, w_router, y and xq_out must be 16-byte aligned
  *   ws          : device workspace of moe_layer_workspace_bytes() bytes,
  *                 zero-filled before its first use and after any call that set
  *                 MOE_DEV_TIMEOUT; completed calls leave it ready for the next
@@ -281,6 +293,9 @@ moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, con
  * MOE_DEV_TIMEOUT in the status word (moe_read_device_status) and returns.
  * Limits as moe_route and moe_expert_ffn; additionally the blocks must all be
  * resident at once (checked: MOE_ERR_UNSUPPORTED otherwise).
+ * Errors: as moe_route and moe_expert_ffn (argument errors before any launch),
+ * and MOE_ERR_UNSUPPORTED for a shared pool whose format is neither the
+ * routed pool's nor Q8_0.
  */
 #define MOE_LAYER_OVERLAP_PREVIOUS 0x1u
 moe_status moe_layer_forward(const float *hidden, int T, const void *w_router, moe_qtype rtype,
@@ -292,7 +307,8 @@ size_t moe_layer_workspace_bytes(int T, int k, const moe_pool *pool, const moe_p
 
 /*
  * Reads (and, if clear != 0, zeroes) the device status word at the start of
- * an FFN workspace.  Synchronises `stream`.  *flags receives MOE_DEV_* bits.
+ * an FFN or layer workspace (both keep it in their first 4 bytes).
+ * Synchronises `stream`.  *flags receives MOE_DEV_* bits.
  * Returns MOE_ERR_DEVICE_STATUS if any bit was set, MOE_OK otherwise.
  */
 moe_status moe_read_device_status(void *ws, int clear, uint32_t *flags, cudaStream_t stream);

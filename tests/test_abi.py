@@ -117,3 +117,29 @@ def test_layer_call_sizes_and_argument_errors():
     odd_shared_h = moe._Pool(moe.Q4_K, 1024, 512, 1, 1 << 21)
     assert call(shared_=odd_shared_h) == INVALID  # the shared expert must match H
     assert call(shared_=odd) == WS
+    mx_shared = moe._Pool(moe.MXFP4, 2048, 512, 1, 1 << 21)
+    assert call(shared_=mx_shared) == UNSUP       # shared: the routed format or Q8_0
+    q8_shared = moe._Pool(moe.Q8_0, 2048, 512, 1, 1 << 21)
+    assert call(shared_=q8_shared) == WS
+
+
+def test_documented_alignment_errors():
+    """Buffers the header marks 16-byte aligned are refused before any launch
+    when they are not."""
+    L = moe.lib()
+    INVALID = 1
+    s = ctypes.c_void_p(0)
+    P = 1 << 20
+    assert L.moe_quantize_q8K(P + 4, 1, 256, P, s) == INVALID          # x
+    assert L.moe_quantize_q8K(P, 1, 256, P + 8, s) == INVALID          # xq
+    args = [P, None, 1, 512, P, moe.F32, 16, None, 2, 0, 1, P, P, None, P, 1 << 16, s]
+    bad_h = list(args); bad_h[0] = P + 4
+    assert L.moe_route(*bad_h) == INVALID                               # hidden, F32 router
+    bad_w = list(args); bad_w[4] = P + 4
+    assert L.moe_route(*bad_w) == INVALID                               # router rows
+    pool = moe._Pool(moe.Q4_K, 2048, 512, 8, P)
+    ffn = [P, 1, P, P, 2, ctypes.byref(pool), None, P, None, 0, s]
+    bad_y = list(ffn); bad_y[7] = P + 4
+    assert L.moe_expert_ffn(*bad_y) == INVALID                          # y
+    bad_x = list(ffn); bad_x[0] = P + 8
+    assert L.moe_expert_ffn(*bad_x) == INVALID                          # xq
