@@ -176,7 +176,11 @@ moe_status moe_route(const float *hidden, const void *xq, int T, int H,
                      void *ws, size_t ws_bytes, cudaStream_t stream);
 size_t moe_route_workspace_bytes(int T, int E, int H);
 
-/* One expert: packed device matrices (moe_pack_weights) and optional biases. */
+/* One expert: packed device matrices (moe_pack_weights) and optional biases.
+ * A fused gate_up tensor (one [2I][H] matrix, gate rows first, as the README's
+ * GGUF notes allow) packed as one matrix serves both projections: gate = its
+ * start, up = gate + moe_packed_bytes(qtype, I, H), since packed tiles of 32
+ * rows are stored one after another. */
 typedef struct {
     const void *gate;     /* packed [I][H]; NULL: this expert is not owned here  */
     const void *up;       /* packed [I][H]                                        */

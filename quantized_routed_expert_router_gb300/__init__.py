@@ -155,13 +155,27 @@ class ExpertPool:
     """A moe_pool: packed expert matrices plus the device pointer table.
 
     entries: list of dicts with packed 'gate', 'up', 'down' tensors (or None
-    for "not mine") and optional 'b_gate', 'b_up', 'b_down' fp32 tensors."""
+    for "not mine") and optional 'b_gate', 'b_up', 'b_down' fp32 tensors.
+    A fused gate_up tensor (GGUF files may store gate and up as one [2I][H]
+    matrix, gate rows first) packed as one matrix is given as 'gate_up': its
+    first moe_packed_bytes(qtype, I, H) bytes are the gate, the rest the up
+    projection (packed tiles of 32 rows are contiguous)."""
 
     def __init__(self, qtype: int, H: int, I: int, entries: list, device=None):
         self.qtype, self.H, self.I, self.E = qtype, H, I, len(entries)
         self._keep = []
         rows = []
         for en in entries:
+            if en is not None and en.get("gate_up") is not None:
+                if en.get("gate") is not None or en.get("up") is not None:
+                    raise ValueError("give either 'gate_up' or 'gate' and 'up'")
+                half = moe_packed_bytes(qtype, I, H)
+                gu = en["gate_up"]
+                if half == 0 or gu.numel() * gu.element_size() != 2 * half:
+                    raise ValueError(f"'gate_up' must hold 2 x {half} packed bytes")
+                flat = gu.reshape(-1).view(torch.uint8)
+                en = dict(en, gate=flat[:half], up=flat[half:])
+                del en["gate_up"]
             if en is None or en.get("gate") is None:
                 rows.append([0] * 6)
                 continue

@@ -143,3 +143,25 @@ def test_documented_alignment_errors():
     assert L.moe_expert_ffn(*bad_y) == INVALID                          # y
     bad_x = list(ffn); bad_x[0] = P + 8
     assert L.moe_expert_ffn(*bad_x) == INVALID                          # xq
+
+
+def test_fused_gate_up_entry_points_into_one_buffer():
+    """A fused gate_up matrix packed as one buffer: the pool's up pointer is the
+    gate pointer plus the packed bytes of I rows (host-side table only)."""
+    import torch
+    H, I = 2048, 512
+    for qt in (moe.Q4_K, moe.Q2_K, moe.Q8_0, moe.MXFP4):
+        half = moe.moe_packed_bytes(qt, I, H)
+        assert half > 0 and half % 16 == 0
+        assert moe.moe_packed_bytes(qt, 2 * I, H) == 2 * half      # 32-row tiles stack
+        gu = torch.zeros(2 * half, dtype=torch.uint8)
+        down = torch.zeros(moe.moe_packed_bytes(qt, H, I), dtype=torch.uint8)
+        pool = moe.ExpertPool(qt, H, I, [dict(gate_up=gu, down=down), None], device="cpu")
+        t = pool.table.tolist()
+        assert t[0][:3] == [gu.data_ptr(), gu.data_ptr() + half, down.data_ptr()]
+        assert t[1] == [0] * 6
+    with pytest.raises(ValueError):
+        moe.ExpertPool(moe.Q4_K, H, I, [dict(gate_up=torch.zeros(10, dtype=torch.uint8), down=down)],
+                       device="cpu")
+    with pytest.raises(ValueError):
+        moe.ExpertPool(moe.Q4_K, H, I, [dict(gate_up=gu, gate=gu, down=down)], device="cpu")
