@@ -39,7 +39,10 @@ def parse():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", default="a3b")
+    p.add_argument("--config", default="a22b")
+    p.add_argument("--also", default="a3b",
+                   help="comma list of further workloads timed after the main one and reported under "
+                        "config.also (T=1, default stack depth); 'none' to skip")
     p.add_argument("--layers", type=int, default=0)
     p.add_argument("--tokens", type=int, default=1)
     p.add_argument("--seed", type=int, default=0)
@@ -250,6 +253,104 @@ def workload_name(cfg, L, T):
     return f"{cfg.name}: {cfg.note}; {L}-layer stack of distinct layers, {T} token(s) per step (decode)"
 
 
+class Stack:
+    """L distinct seeded layers of one workload on the device, captured as
+    CUDA graphs: one fused launch per layer ("step"), the three calls per
+    layer ("three") and the FFN call alone ("ffn")."""
+
+    def __init__(self, cfg, L, T, seed, dev, stream, overlap, keep_host=0):
+        import torch
+        import synth
+        import quantized_routed_expert_router_gb300 as moe
+        from quantized_routed_expert_router_gb300.device_layer import DeviceLayer
+        self.cfg, self.L, self.T = cfg, L, T
+        t_gen = time.perf_counter()
+        self.layers, self.host_sample = [], []
+        for l in range(L):
+            Lh = synth.make_layer(cfg, l, T=T, seed=seed)
+            self.layers.append(DeviceLayer(Lh, dev))
+            if l < keep_host:
+                self.host_sample.append(Lh)
+            del Lh
+        # one contiguous input and output buffer for the whole stack, so the
+        # end-to-end leg moves each step's inputs and results in one copy each
+        self.X = torch.empty((L, T, cfg.H), dtype=torch.float32, device=dev)
+        self.Y = torch.empty((L, T, cfg.H), dtype=torch.float32, device=dev)
+        for l, dl in enumerate(self.layers):
+            self.X[l].copy_(dl.x)
+            dl.x, dl.y = self.X[l], self.Y[l]
+        torch.cuda.synchronize()
+        self.gen_s = time.perf_counter() - t_gen
+        flags = moe.LAYER_OVERLAP_PREVIOUS if overlap else 0
+
+        def step_fused():
+            for dl in self.layers:
+                dl.forward_fused(flags=flags, outputs=False)
+
+        def step_three(ffn_only=False):
+            for dl in self.layers:
+                if not ffn_only:
+                    dl.quantize()
+                    dl.route(logits=False)
+                dl.ffn()
+
+        with torch.cuda.stream(stream):
+            step_three()                  # eager once: kernel attributes, ids for the byte count
+            step_fused()
+        torch.cuda.synchronize()
+        bad = [moe.moe_read_device_status(dl.ws_layer) for dl in self.layers]
+        if any(bad):
+            raise RuntimeError(f"device status after the first fused step: {bad}")
+        self.bytes_l = [layer_bytes(cfg, dl, moe) for dl in self.layers]
+        self.step_bytes = sum(b["total"] for b in self.bytes_l)
+        self.graphs = {}
+        for name, fn in (("step", step_fused), ("three", step_three), ("ffn", lambda: step_three(ffn_only=True))):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            self.graphs[name] = g
+        torch.cuda.synchronize()
+
+    def status(self):
+        import quantized_routed_expert_router_gb300 as moe
+        return [moe.moe_read_device_status(dl.ws_layer) for dl in self.layers]
+
+
+def timed(g, K, W, stream, world, dev):
+    """Device milliseconds of K graph replays after W untimed ones, max over ranks."""
+    import torch
+    import torch.distributed as dist
+    for _ in range(W):
+        g.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    return max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+
+def side_figures(S, K, W, stream, world, dev, peak):
+    """A further workload's fused-stack figures (reported beside the main line)."""
+    ms = timed(S.graphs["step"], K, W, stream, world, dev)
+    st = S.status()
+    if any(st):
+        raise RuntimeError(f"device status after the timed region ({S.cfg.name}): {st}")
+    us = 1e3 * ms / (K * S.L)
+    gbs = (S.step_bytes / S.L) / (us / 1e6) / 1e9
+    return {"workload": workload_name(S.cfg, S.L, S.T), "steps": K, "layer_tok_s": job_throughput(
+        world, K, S.L, S.T, ms / 1e3), "us_per_layer": us, "bytes_per_layer": S.step_bytes / S.L,
+        "hbm_gbs": gbs, "hbm_frac_of_measured": gbs / peak, "setup_s": S.gen_s}
+
+
 def main():
     args = parse()
     import synth
@@ -263,95 +364,32 @@ def main():
     import torch.distributed as dist
     from quantized_routed_expert_router_gb300 import _build
     _build.build()
-    import quantized_routed_expert_router_gb300 as moe
-    from quantized_routed_expert_router_gb300.device_layer import DeviceLayer
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     T = args.tokens
+    stream = torch.cuda.Stream(device=dev)
+    peak, peak_src = peaks()
 
     # ---- workload: L distinct layers, each rank its own tokens (seed offset)
-    t_gen = time.perf_counter()
-    layers, host_sample = [], []
-    for l in range(L):
-        Lh = synth.make_layer(cfg, l, T=T, seed=rank_seed(args.seed, rank))
-        layers.append(DeviceLayer(Lh, dev))
-        if l < 2 and world == 1 and not args.no_cpu:
-            host_sample.append(Lh)
-        del Lh
-    # one contiguous input and output buffer for the whole stack, so the
-    # end-to-end leg moves each step's inputs and results in one copy each
-    X = torch.empty((L, T, cfg.H), dtype=torch.float32, device=dev)
-    Y = torch.empty((L, T, cfg.H), dtype=torch.float32, device=dev)
-    for l, dl in enumerate(layers):
-        X[l].copy_(dl.x)
-        dl.x, dl.y = X[l], Y[l]
-    torch.cuda.synchronize()
-    gen_s = time.perf_counter() - t_gen
-    stream = torch.cuda.Stream(device=dev)
-
-    flags = 0 if args.no_overlap else moe.LAYER_OVERLAP_PREVIOUS
-
-    def step_fused():
-        for dl in layers:
-            dl.forward_fused(flags=flags, outputs=False)
-
-    def step_three(ffn_only=False):
-        for dl in layers:
-            if not ffn_only:
-                dl.quantize()
-                dl.route(logits=False)
-            dl.ffn()
-
-    with torch.cuda.stream(stream):
-        step_three()                  # eager once: kernel attributes, ids for the byte count
-        step_fused()
-    torch.cuda.synchronize()
-    bad = [moe.moe_read_device_status(dl.ws_layer) for dl in layers]
-    if any(bad):
-        raise RuntimeError(f"device status after the first fused step: {bad}")
-    bytes_l = [layer_bytes(cfg, dl, moe) for dl in layers]
-    step_bytes = sum(b["total"] for b in bytes_l)
-    ffn_bytes = sum(b["experts"] + b["shared"] for b in bytes_l)
-
-    graphs = {}
-    for name, fn in (("step", step_fused), ("three", step_three), ("ffn", lambda: step_three(ffn_only=True))):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            fn()
-        graphs[name] = g
-    torch.cuda.synchronize()
-
-    def timed(g, K, W):
-        for _ in range(W):
-            g.replay()
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(K):
-                g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        return max_over_ranks(e0.elapsed_time(e1), world, dev)
+    keep = 2 if (world == 1 and not args.no_cpu) else 0
+    S = Stack(cfg, L, T, rank_seed(args.seed, rank), dev, stream, not args.no_overlap, keep_host=keep)
+    layers, X, Y = S.layers, S.X, S.Y
+    bytes_l, step_bytes = S.bytes_l, S.step_bytes
+    graphs = S.graphs
 
     K, W = args.steps, max(3, args.warmup)
     with ClockSampler(local) as cs:
-        ms = timed(graphs["step"], K, W)
+        ms = timed(graphs["step"], K, W, stream, world, dev)
     clocks = cs.summary()
-    status = [moe.moe_read_device_status(dl.ws_layer) for dl in layers]
+    status = S.status()
     if any(status):
         raise RuntimeError(f"device status after the timed region: {status}")
     K3 = max(3, K // 4)
-    ms_three = timed(graphs["three"], K3, W)
-    ms_ffn = timed(graphs["ffn"], K3, W)
+    ms_three = timed(graphs["three"], K3, W, stream, world, dev)
+    ms_ffn = timed(graphs["ffn"], K3, W, stream, world, dev)
 
     # ---- end to end through the public API: pinned H2D of every layer's input,
     # the captured public-API calls, D2H of every layer's y, per step
@@ -376,20 +414,29 @@ def main():
                "d2h_bytes_per_step": L * T * cfg.H * 4, "steps": ke,
                "mode": "pinned H2D + graph replay of the public C-ABI calls + D2H + stream sync, wall clock"}
 
+    # ---- further workloads, reported beside the main line (not the headline)
+    also = {}
+    for name in [a for a in args.also.split(",") if a and a != "none" and a != args.config]:
+        c2 = synth.CONFIGS[name]
+        S2 = Stack(c2, DEFAULT_LAYERS.get(name, c2.layers), 1, rank_seed(args.seed, rank), dev, stream,
+                   not args.no_overlap)
+        also[name] = side_figures(S2, K, W, stream, world, dev, peak)
+        del S2
+        torch.cuda.empty_cache()
+
     value = job_throughput(world, K, L, T, ms / 1e3)
-    peak, peak_src = peaks()
     launch_ms = ms / (K * L)
     achieved = (step_bytes / L) / (launch_ms / 1e3) / 1e9
     traffic = traffic_record(f"layer_kernel:{cfg.name}:T{T}")
     cpu = None
-    if world == 1 and not args.no_cpu and host_sample:
+    if world == 1 and not args.no_cpu and S.host_sample:
         # after every GPU leg, so the host threads disturb no GPU timing
-        n1, dt1 = time_oracle(host_sample, 1, steps=100000, seconds=4.0)
+        n1, dt1 = time_oracle(S.host_sample, 1, steps=100000, seconds=4.0)
         C = host_threads()
-        n, dt = time_oracle(host_sample, C, steps=100000, seconds=6.0)
+        n, dt = time_oracle(S.host_sample, C, steps=100000, seconds=6.0)
         cpu = {"value": n * T / dt, "unit": UNIT, "cores": C, "kind": "oracle",
                "sample": f"{n} layer-steps of {cfg.name} (T={T}) on {C} host threads at once over "
-                         f"{len(host_sample)} seeded layers, scalar C oracle, {dt:.1f} s",
+                         f"{len(S.host_sample)} seeded layers, scalar C oracle, {dt:.1f} s",
                "single_thread": {"value": n1 * T / dt1, "cores": 1,
                                  "sample": f"{n1} layer-steps on one thread, {dt1:.1f} s"}}
     if rank == 0:
@@ -411,7 +458,8 @@ def main():
                                + ("" if args.no_overlap else ", overlap flag (programmatic dependent launch)"),
                        "three_call_us_per_layer": 1e3 * ms_three / (K3 * L),
                        "three_call_ffn_us_per_layer": 1e3 * ms_ffn / (K3 * L),
-                       "setup_s": gen_s},
+                       "setup_s": S.gen_s,
+                       "also": also},
             "roofline": {"bound": "hbm", "kernel": "layer_kernel (moe_layer_forward)",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_source": peak_src, "traffic": traffic,

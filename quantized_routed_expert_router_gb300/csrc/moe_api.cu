@@ -58,6 +58,20 @@ bool pool_shape_ok(const moe_pool *p) {
 
 }  // namespace
 
+namespace moe {
+moe_status ffn_check_args(const void *xq, int T, const int32_t *ids, const float *weights, int k,
+                          const moe_pool *pool, const moe_pool *shared, const float *y) {
+    if (T < 0 || T > MOE_MAX_TOKENS || k < 1 || k > MOE_MAX_K) return MOE_ERR_INVALID_ARG;
+    if (!pool_ok(pool, false)) return MOE_ERR_INVALID_ARG;
+    if (shared && !pool_ok(shared, true)) return MOE_ERR_INVALID_ARG;
+    if (!pool_shape_ok(pool)) return MOE_ERR_UNSUPPORTED;
+    if (shared && (shared->H != pool->H || !pool_shape_ok(shared))) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!xq || !ids || !weights || !y || !aligned16(xq) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+}  // namespace moe
+
 extern "C" {
 
 int moe_act_block(int n) { return act_block(n); }
@@ -132,13 +146,8 @@ size_t moe_ffn_workspace_bytes(int T, int k, const moe_pool *pool, const moe_poo
 moe_status moe_expert_ffn(const void *xq, int T, const int32_t *ids, const float *weights, int k,
                           const moe_pool *pool, const moe_pool *shared, float *y, void *ws, size_t ws_bytes,
                           cudaStream_t stream) {
-    if (T < 0 || T > MOE_MAX_TOKENS || k < 1 || k > MOE_MAX_K) return MOE_ERR_INVALID_ARG;
-    if (!pool_ok(pool, false)) return MOE_ERR_INVALID_ARG;
-    if (shared && !pool_ok(shared, true)) return MOE_ERR_INVALID_ARG;
-    if (!pool_shape_ok(pool)) return MOE_ERR_UNSUPPORTED;
-    if (shared && (shared->H != pool->H || !pool_shape_ok(shared))) return MOE_ERR_UNSUPPORTED;
-    if (T == 0) return MOE_OK;
-    if (!xq || !ids || !weights || !y || !aligned16(xq) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    const moe_status v = moe::ffn_check_args(xq, T, ids, weights, k, pool, shared, y);
+    if (v != MOE_OK || T == 0) return v;
     const FfnWs L = ffn_ws_layout(T, k, pool->H, pool->I, shared ? shared->I : 0);
     if (!ws || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
     char *w = (char *)ws;

@@ -18,9 +18,9 @@
 //     (token, slot) pairs by expert and derives the same work plan:
 //       A units = (expert, 32-row tile of I): gate + up records,
 //       B units = (expert, 32-row tile of H): down records.
-//     A units are dealt out in a snake over blocks; for one token the B
-//     units continue the snake, otherwise they are contiguous ranges sized
-//     so every block streams about the same number of bytes.
+//     A units are dealt out in a snake over blocks; B units go in
+//     contiguous ranges sized so every block streams about the same number
+//     of bytes (so a block's B units need the h of one or two experts).
 //  4. The producer streams the units' records (TMA bulk copies, complete_tx
 //     mbarriers) through a byte ring, up to eight records per copy; consumer
 //     warp r % 8 takes record r of an A unit, and a batch's B records are
@@ -36,8 +36,9 @@
 //  until they carry the epoch.  An 8-byte aligned
 //  access is single-copy atomic, so a word with the right epoch holds the
 //  right value and no fence is needed on either side.  The epoch is a counter
-//  in the workspace: read after the dependency wait, written back (+1) by
-//  block 0 at its end.
+//  in the workspace, read by every block after the dependency wait; the last
+//  block to read it (an arrival count beside it) writes it back (+1), so no
+//  block can see the next value early.
 //  Every wait is bounded (SM cycle counter); a timeout sets MOE_DEV_TIMEOUT,
 //  drains this block's copies in flight and returns.
 #pragma once
@@ -49,10 +50,17 @@
 
 namespace moe {
 
-constexpr int LW = 8;                  // consumer warps
-constexpr int LT = (LW + 1) * 32;      // threads per block (with the producer warp)
+// consumer warps: 16 for one token (four per SM sub-partition keep the
+// integer dots' latencies covered), 8 for four tokens (four times the dot
+// work per record and per register)
+template <int NT>
+struct Warps {
+    static constexpr int LW = NT == 1 ? 16 : 8;
+    static constexpr int LT = (LW + 1) * 32;   // threads per block (with the producer warp)
+};
+constexpr int MAX_LW = 16;
 constexpr int NBAR = 32;               // ring items in flight (barrier slots)
-constexpr int MAX_ITEM_RECS = 8;       // records per ring item, at most (also the empty-barrier count)
+constexpr int MAX_ITEM_RECS = 16;      // records per ring item, at most (also the empty-barrier count)
 // bound on every device-side wait, in SM clock cycles (about 0.4-1 s at the
 // clocks this part runs at); the cycle counter is cheap to poll
 constexpr long long WAIT_CYCLES = 800ll * 1000ll * 1000ll;
@@ -94,6 +102,22 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         "l"(src), "r"(bytes), "r"(saddr(bar))
         : "memory");
 }
+// Weight records and router rows are read once per launch: their L2 lines
+// are marked evict-first, so the stream does not push out what the launch
+// re-reads (exchange words, activations, expert tables, the kernel's code).
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void bulk_g2s_stream(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                                uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(saddr(dst)),
+        "l"(src), "r"(bytes), "r"(saddr(bar)), "l"(pol)
+        : "memory");
+}
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 // tagged word: the value's bits in the low half, the epoch in the high half
@@ -121,7 +145,19 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const unsigned *p) {
 __device__ __forceinline__ void st_relaxed_u32(unsigned *p, uint32_t v) {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }   // consumers only
+// This launch's epoch: the stored counter + 1.  Each block then counts its
+// read (acq_rel: the read is ordered before the count).  The count's result
+// is only looked at when the block ends (finish), so the round trip stays off
+// the routing path; the block that completed the count has seen every
+// block's read, and stores the new epoch and clears the count for the next
+// launch, which reads both only after this grid is done.
+__device__ __forceinline__ uint32_t count_epoch_read(unsigned *arrive) {
+    uint32_t n;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(n) : "l"(arrive) : "memory");
+    return n;
+}
+template <int LW>
+__device__ __forceinline__ void cbar_n() { asm volatile("bar.sync 1, %0;" ::"n"(LW * 32) : "memory"); }   // consumers only
 
 // ------------------------------------------------------------- block state
 
@@ -134,12 +170,14 @@ struct Misc {
     uint32_t bitmap[MOE_MAX_EXPERTS / 32];
     int wpre[MOE_MAX_EXPERTS / 32];
     int nkeys, kkey[64], kslot[64];   // experts of the current B batch and their hq slots
-    int bsnake, bp0, nb, bend;         // this block's B units: snake passes from bp0, or [jb0, jb1)
+    int nb, bend;                      // this block's B units: [jb0, jb1), nb of them; end of the hq batch
     // the current hq batch's B units (at most 64): unit index, first ring
     // item and first record (relative to the batch; entry [n] holds the
     // totals) and hq slot
     int bt_j[64], bt_it[65], bt_rec[65], bt_slot[64];
-    unsigned long long bsum[LW], target, lo, hi;
+    uint32_t bsum[MAX_LW], target, lo, hi;   // B shares, in 128-byte lines
+    int closed;          // the B shares need no clamping (closed form)
+    int brev;            // B ranges are given to blocks G-1 first
 };
 
 static_assert(sizeof(Misc) <= kLayerMiscBytes, "fused kernel block state outgrew its shared-memory region");
@@ -189,11 +227,15 @@ extern __shared__ __align__(128) unsigned char moe_smem[];
 // (record i at shared offset abase + aidx[i] * astride): integer sub-block
 // dots, accumulated in record order into acc[i].  Used by the gate, up and
 // down projections.
-template <class FF, int NT>
-static __device__ __forceinline__ void rec_dot(uint32_t rec, int nb, int k0, int cols, uint32_t abase, uint32_t astride,
-                                            const int *aidx, int nt, int lane, float *acc) {
-    typename FF::W w;
+// The record is pulled into registers (w) first, so its ring slot can be
+// released before the dots run (rec_load, then rec_dot_w).
+template <class FF>
+static __device__ __forceinline__ void rec_load(typename FF::W &w, uint32_t rec, int nb, int lane) {
     FF::load_s(w, moe_smem + rec, nb, lane);
+}
+template <class FF, int NT>
+static __device__ __forceinline__ void rec_dot_w(const typename FF::W &w, int nb, int k0, int cols, uint32_t abase,
+                                              uint32_t astride, const int *aidx, int nt, float *acc) {
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
         if (i < nt) {
@@ -227,7 +269,7 @@ struct Plan {
     int n_sa, nA, n_sb, nB;      // A units: shared then routed; B units: shared then routed
     int tilesI, tilesIs, tilesH; // 32-row tiles of I, of the shared expert's I, of H
     float invI, invH;            // 1 / tilesI, 1 / tilesH (quotients corrected exactly)
-    int bsnake, bp0, nb, jb0;    // this block's B units: snake passes from bp0, or [jb0, jb0 + nb)
+    int nb, jb0;                 // this block's B units: [jb0, jb0 + nb)
 };
 
 // q / t for 0 <= q < 2^22, t >= 1, from a float estimate corrected exactly
@@ -240,12 +282,15 @@ __device__ __forceinline__ int div_tiles(int q, int t, float inv) {
 
 template <class F, class FS, int NT>
 struct LayerKernel {
+    static constexpr int LW = Warps<NT>::LW, LT = Warps<NT>::LT;
+    __device__ static void cbar() { cbar_n<LW>(); }
     const LayerArgs &a;
     unsigned char *sm;
     Smem o;
     Misc *m;
     int c, G, warp, lane;
     uint32_t ep = 0;   // consumers: this launch's epoch (after the dependency wait)
+    uint32_t arrived = 0;   // thread 0: blocks that had read the epoch before this one
     Plan p;            // loaded by load_plan once the plan is in shared memory
     // the shared expert's table entry: the caller's device table until the
     // routing handoff, then the block's shared-memory copy of it
@@ -263,6 +308,10 @@ struct LayerKernel {
     __device__ uint64_t *full_bar(int i) { return reinterpret_cast<uint64_t *>(sm + o.bars) + (i % NBAR); }
     __device__ uint64_t *empty_bar(int i) { return reinterpret_cast<uint64_t *>(sm + o.bars) + NBAR + (i % NBAR); }
     __device__ uint64_t *fixed_bar() { return reinterpret_cast<uint64_t *>(sm + o.bars) + 2 * NBAR; }
+    // A-unit partial sums, two buffers: ready (every consumer warp has
+    // written its partials) and free (the unit's reducing warp has read them)
+    __device__ uint64_t *ready_bar(int b) { return reinterpret_cast<uint64_t *>(sm + o.bars) + 2 * NBAR + 1 + b; }
+    __device__ uint64_t *free_bar(int b) { return reinterpret_cast<uint64_t *>(sm + o.bars) + 2 * NBAR + 3 + b; }
     __device__ uint32_t *starts() { return reinterpret_cast<uint32_t *>(sm + o.starts); }
     // item index currently owning each ring slot (set by the producer once the
     // slot's previous item is reclaimed); lets a consumer that is many items
@@ -294,8 +343,6 @@ struct LayerKernel {
         p.tilesH = a.H / 32;
         p.invI = 1.f / (float)p.tilesI;
         p.invH = 1.f / (float)p.tilesH;
-        p.bsnake = m->bsnake;
-        p.bp0 = m->bp0;
         p.nb = m->nb;
         p.jb0 = m->jb0;
     }
@@ -377,6 +424,7 @@ struct LayerKernel {
     struct Ring {
         uint32_t head;
         int issued, tail;   // items issued so far; oldest item not yet reclaimed
+        uint64_t pol;       // L2 policy of the weight stream
     };
 
     __device__ bool reclaim_oldest(Ring &R) {
@@ -419,26 +467,27 @@ struct LayerKernel {
         uint8_t *dst = sm + o.ring + start;
         uint64_t *fb = full_bar(i);
         mbar_arm(fb, bytes);
-        // consumers arrive once per record of the item
-        const uint32_t users = (uint32_t)(r1 - r0);
+        // consumers arrive once per record of the item (an A item holds a
+        // gate and an up record per row range)
+        const uint32_t users = (uint32_t)((U.kind <= 1 ? 2 : 1) * (r1 - r0));
         if (users < MAX_ITEM_RECS) mbar_arrive_n(empty_bar(i), MAX_ITEM_RECS - users);
         if (U.kind == 0 || U.kind == 1) {
             const size_t off = U.kind == 0 ? FS::rec_off(a.H, r0) : F::rec_off(a.H, r0);
-            bulk_g2s(dst, U.g + off, run, fb);
-            bulk_g2s(dst + run, U.up + off, run, fb);
+            bulk_g2s_stream(dst, U.g + off, run, fb, R.pol);
+            bulk_g2s_stream(dst + run, U.up + off, run, fb, R.pol);
         } else {
             const size_t off = U.kind == 2 ? FS::rec_off(a.Is, r0) : F::rec_off(a.I, r0);
-            bulk_g2s(dst, U.d + off, run, fb);
+            bulk_g2s_stream(dst, U.d + off, run, fb, R.pol);
         }
         R.head = start + bytes;
         ++R.issued;
         return true;
     }
 
-    __device__ bool issue_unit(Ring &R, int j) {
+    __device__ bool issue_unit(Ring &R, int j, int q0 = 0) {
         Unit U;
         unit_of(j, U);
-        for (int q = 0; q < U.nitems; ++q) {
+        for (int q = q0; q < U.nitems; ++q) {
             if (m->abort) return false;
             if (!issue(R, U, q)) { fail(); return false; }
         }
@@ -462,9 +511,13 @@ struct LayerKernel {
         if (lane == 0) mbar_arrive_n(empty_bar(i), n);
     }
 
-    // A unit: g and u partial sums of this warp's records, then h rows
+    // A unit: g and u partial sums of this warp's records, then h rows.  No
+    // block-wide barrier per unit: each warp leaves its partials in buffer
+    // ua % 2 and goes on to its next unit; the unit's reducing warp (ua % LW)
+    // waits for all of them, writes h and hands the buffer back.  A warp
+    // reuses a buffer only after the reducer of its previous use is done.
     template <class FF>
-    __device__ void run_A(const Unit &U, int &item, int &rbuf) {
+    __device__ void run_A(const Unit &U, int &item, int &ua) {
         float ag[NT], au[NT];
 #pragma unroll
         for (int i = 0; i < NT; ++i) { ag[i] = 0.f; au[i] = 0.f; }
@@ -472,6 +525,8 @@ struct LayerKernel {
 #pragma unroll
         for (int i = 0; i < NT; ++i)
             tok[i] = (i < U.nt) ? (U.kind == 0 ? i : plist()[uoff()[U.u] + i] / a.k) : 0;
+        // Record r's gate and up records both go to warp r % LW, which frees
+        // the ring slot once it has read them both (during the up dot).
         for (int r = warp; r < U.nrec; r += LW) {
             int r0, r1;
             item_recs(U, r >> a.lgra, r0, r1);
@@ -482,22 +537,26 @@ struct LayerKernel {
             const uint8_t *rec_up = base + run_off<FF>(a.H, r0, r1) + run_off<FF>(a.H, r0, r);
             const int nb = FF::rec_blocks(a.H, r);
             const int k0 = r * FF::QK;
-            rec_dot<FF, NT>((uint32_t)(rec - sm), nb, k0, a.H, o.xq, (uint32_t)a.xrec, tok, U.nt, lane, ag);
-            rec_dot<FF, NT>((uint32_t)(rec_up - sm), nb, k0, a.H, o.xq, (uint32_t)a.xrec, tok, U.nt, lane, au);
-            free_item(it);
+            typename FF::W w;
+            rec_load<FF>(w, (uint32_t)(rec - sm), nb, lane);
+            rec_dot_w<FF, NT>(w, nb, k0, a.H, o.xq, (uint32_t)a.xrec, tok, U.nt, ag);
+            rec_load<FF>(w, (uint32_t)(rec_up - sm), nb, lane);
+            free_item(it, 2);
+            rec_dot_w<FF, NT>(w, nb, k0, a.H, o.xq, (uint32_t)a.xrec, tok, U.nt, au);
         }
         item += U.nitems;
-        // NT <= 4: two reduction buffers alternate; NT = 16: one buffer, and
-        // the barrier below keeps it until warp 0 has read the previous unit
-        if (NT > 4) cbar();
-        float *red = reinterpret_cast<float *>(sm + o.red) + (NT <= 4 ? rbuf : 0) * (LW * 2 * NT * 32);
+        const int b = ua & 1, use = ua >> 1;
+        float *red = reinterpret_cast<float *>(sm + o.red) + b * (LW * 2 * NT * 32);
+        if (use > 0 && !m->abort && !mbar_wait(free_bar(b), (uint32_t)((use - 1) & 1))) fail();
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
             red[((warp * 2 + 0) * NT + i) * 32 + lane] = ag[i];
             red[((warp * 2 + 1) * NT + i) * 32 + lane] = au[i];
         }
-        cbar();
-        if (warp == 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_n(ready_bar(b), 1);
+        if (warp == ua % LW) {
+            if (!m->abort && !mbar_wait(ready_bar(b), (uint32_t)(use & 1))) fail();
             const int row = U.rt * 32 + lane;
             const int Irows = U.kind == 0 ? a.Is : a.I;
             tword *hb = U.kind == 0 ? a.h_s : a.h_r;
@@ -514,8 +573,10 @@ struct LayerKernel {
                 const int dest = U.kind == 0 ? i : plist()[uoff()[U.u] + i];
                 st_tag(hb + (size_t)dest * Irows + row, h, ep);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_n(free_bar(b), 1);
         }
-        rbuf ^= 1;
+        ++ua;
     }
 
     // ---------------------------------------------------------- B phase
@@ -661,10 +722,12 @@ struct LayerKernel {
             item_recs(U, q, r0, r1);
             const uint8_t *base = wait_item(item + q);
             if (!base) continue;
-            for (int r = r0; r < r1; ++r)
-                rec_dot<FF, NT>((uint32_t)(base - sm + run_off<FF>(Irows, r0, r)), FF::rec_blocks(Irows, r), r * FF::QK,
-                                Irows, o.hq, (uint32_t)a.hrec, sidx, U.nt, lane, ao);
-            free_item(item + q, (uint32_t)(r1 - r0));
+            for (int r = r0; r < r1; ++r) {
+                typename FF::W w;
+                rec_load<FF>(w, (uint32_t)(base - sm + run_off<FF>(Irows, r0, r)), FF::rec_blocks(Irows, r), lane);
+                if (r + 1 == r1) free_item(item + q, (uint32_t)(r1 - r0));
+                rec_dot_w<FF, NT>(w, FF::rec_blocks(Irows, r), r * FF::QK, Irows, o.hq, (uint32_t)a.hrec, sidx, U.nt, ao);
+            }
         }
         store_o(U, ao);
     }
@@ -699,9 +762,10 @@ struct LayerKernel {
         for (int i = 0; i < NT; ++i) { pt[i] = 0.f; sidx[i] = slot0 + i; }
         const uint8_t *base = wait_item(it0 + q);
         if (base) {
-            rec_dot<FF, NT>((uint32_t)(base - sm + run_off<FF>(Irows, r0, r)), FF::rec_blocks(Irows, r), r * FF::QK,
-                            Irows, o.hq, (uint32_t)a.hrec, sidx, U.nt, lane, pt);
+            typename FF::W w;
+            rec_load<FF>(w, (uint32_t)(base - sm + run_off<FF>(Irows, r0, r)), FF::rec_blocks(Irows, r), lane);
             free_item(it0 + q);
+            rec_dot_w<FF, NT>(w, FF::rec_blocks(Irows, r), r * FF::QK, Irows, o.hq, (uint32_t)a.hrec, sidx, U.nt, pt);
         }
         float *part = reinterpret_cast<float *>(sm + o.red);
 #pragma unroll
@@ -743,18 +807,19 @@ struct LayerKernel {
         if (lane == 0) { m->bt_rec[64] = carry_r; m->bt_it[64] = carry_i; }
     }
 
-    // B units of one hq batch.  Groups of whole units with at most LW records
-    // in all (or one unit) are spread record by record over the warps: each
-    // record's partial sums go to a slot of the reduction buffer, then one
-    // warp per unit adds its slots in record order and writes the o rows.  A
-    // unit with more records than the buffer has slots runs on one warp.
+    // B units of one hq batch.  Groups of whole units with at most a.bslots
+    // records in all (or one unit) are spread record by record over the
+    // warps (record t of the group to warp t % 8, each warp in record order):
+    // each record's partial sums go to a slot of the reduction buffer, then
+    // one warp per unit adds its slots in record order and writes the o rows.
+    // A unit with more records than the buffer has slots runs on one warp.
     __device__ void run_B_batch(int n, int n1, int &item) {
-        constexpr int CAP = NT <= 4 ? 32 : 16;   // record slots in the reduction buffer
+        const int CAP = a.bslots;   // record slots in the reduction buffer
         const int nu = n1 - n;   // the unit table was built by load_hq_batch
         const int *brec = m->bt_rec;
         for (int k = 0; k < nu;) {
             int ke = k + 1;
-            while (ke < nu && brec[ke + 1] - brec[k] <= LW) ++ke;
+            while (ke < nu && brec[ke + 1] - brec[k] <= CAP) ++ke;
             const int recs = brec[ke] - brec[k];
             if (recs > CAP) {   // one long unit: the warp-per-unit path
                 if (warp == 0) {
@@ -766,8 +831,8 @@ struct LayerKernel {
                 k = ke;
                 continue;
             }
+            int kk = k;
             for (int t = warp; t < recs; t += LW) {
-                int kk = k;
                 while (brec[kk + 1] - brec[k] <= t) ++kk;
                 Unit U;
                 unit_of(m->bt_j[kk], U);
@@ -870,6 +935,10 @@ struct LayerKernel {
             for (int i = 0; i < NBAR; ++i) mbar_init(full_bar(i), 1);
             for (int i = 0; i < NBAR; ++i) mbar_init(empty_bar(i), MAX_ITEM_RECS);
             mbar_init(fixed_bar(), 1);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(ready_bar(b), LW);
+                mbar_init(free_bar(b), 1);
+            }
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             m->abort = 0;
         }
@@ -883,9 +952,10 @@ struct LayerKernel {
         e1 = (int)(((long long)(c + 1) * a.E) / G);
     }
 
-    __device__ void quantise_x() {
+    // x into q8 records by consumer warps w0 .. LW-1
+    __device__ void quantise_x(int w0) {
         const int chunks = (a.H + 255) / 256;
-        for (int w = warp; w < a.T * chunks; w += LW) {
+        for (int w = warp - w0; w < a.T * chunks; w += LW - w0) {
             const int t = w / chunks, ch = w - t * chunks;
             float v[8];
             const bool act = quant_load8<false>(a.x + (size_t)t * a.H, a.H, 256 * ch, lane, v);
@@ -1007,7 +1077,7 @@ struct LayerKernel {
         myid = lane == s ? win : myid;
         mykey = lane == s ? mx : mykey;
     }
-    template <int JN, int K>
+    template <int JN>
     __device__ float select_topk(const float *lg, int *out) {
         uint32_t key[JN];   // 0 marks padding (every real logit's key is > 0)
 #pragma unroll
@@ -1020,45 +1090,37 @@ struct LayerKernel {
         // rounds as a loop, not unrolled: this code runs once per launch and
         // fetching it cold costs more than the loop's own instructions
 #pragma unroll 1
-        for (int s = 0; s < (K > 0 ? K : a.k); ++s) topk_round<JN>(key, s, myid, mykey);
+        for (int s = 0; s < a.k; ++s) topk_round<JN>(key, s, myid, mykey);
         if (lane < a.k) out[lane] = myid;
         return fkey_value(mykey);
     }
-    template <int JN>
-    __device__ float select_topk_k(const float *lg, int *out) {
-        switch (a.k) {
-            case 8: return select_topk<JN, 8>(lg, out);
-            case 4: return select_topk<JN, 4>(lg, out);
-            case 2: return select_topk<JN, 2>(lg, out);
-            default: return select_topk<JN, 0>(lg, out);
-        }
-    }
 
-    // every logit: each consumer thread loads its words (up to 8) at once and
-    // re-reads the ones not yet published, in rounds
-    __device__ void topk_and_group() {
+    // every logit into shared memory: thread i of n loads words i, i + n, ...
+    // (up to 8 per round trip) and re-reads the ones not yet published
+    __device__ void poll_logits(int i, int n) {
         float *lgs = reinterpret_cast<float *>(sm + o.lg);
         const int TE = a.T * a.E;
-        for (int i0 = threadIdx.x; i0 < TE; i0 += 8 * LW * 32) {
-            const int n = min(8, (TE - i0 + LW * 32 - 1) / (LW * 32));
+        for (int i0 = i; i0 < TE; i0 += 8 * n) {
+            const int cnt = min(8, (TE - i0 + n - 1) / n);
             tword w[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-                if (q < n) w[q] = ld_tag(a.logits + i0 + q * LW * 32);
+                if (q < cnt) w[q] = ld_tag(a.logits + i0 + q * n);
             {   // re-read every missing word per round: one round trip each
                 bool all = true;
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    if (q < n) all &= tag_of(w[q]) == ep;
+                    if (q < cnt) all &= tag_of(w[q]) == ep;
                 const long long t0 = clock64();
                 while (!all) {
+                    __nanosleep(128);   // many blocks poll the same few lines: ease off between rounds
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
-                        if (q < n && tag_of(w[q]) != ep) w[q] = ld_tag(a.logits + i0 + q * LW * 32);
+                        if (q < cnt && tag_of(w[q]) != ep) w[q] = ld_tag(a.logits + i0 + q * n);
                     all = true;
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
-                        if (q < n) all &= tag_of(w[q]) == ep;
+                        if (q < cnt) all &= tag_of(w[q]) == ep;
                     if (!all && (m->abort || clock64() - t0 > WAIT_CYCLES)) {
                         fail();
                         break;
@@ -1067,14 +1129,28 @@ struct LayerKernel {
             }
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-                if (q < n) lgs[i0 + q * LW * 32] = tag_value(w[q]);
+                if (q < cnt) lgs[i0 + q * n] = tag_value(w[q]);
         }
-        cbar();
-        for (int t = warp; t < a.T; t += LW) {
-            const float *lg = lgs + (size_t)t * a.E;
-            const float mysel = a.E <= 256 ? select_topk_k<8>(lg, ids() + t * a.k) : select_topk_k<32>(lg, ids() + t * a.k);
-            if (lane < a.k) wts()[t * a.k + lane] = mysel;   // the weights replace these later
-        }
+    }
+    // token t's top-k by the calling warp
+    __device__ void topk_token(int t) {
+        const float *lg = reinterpret_cast<const float *>(sm + o.lg) + (size_t)t * a.E;
+        const float mysel = a.E <= 256 ? select_topk<8>(lg, ids() + t * a.k) : select_topk<32>(lg, ids() + t * a.k);
+        if (lane < a.k) wts()[t * a.k + lane] = mysel;   // the weights replace these later
+    }
+
+    // After the logits are published: every logit read back, the top-k of
+    // each token, x quantised (fp32 router; a Q8_0 router quantised it
+    // before), then the grouping and the work plan.  One token: warp 0 reads
+    // the logits and selects while the other warps quantise x.
+    __device__ void route_tail(bool x_done) {
+        // (one call site per step: every inlined copy is code each launch fetches)
+        const bool split = NT == 1 && !x_done;
+        if (!x_done && (!split || warp > 0)) quantise_x(split ? 1 : 0);
+        if (!split || warp == 0) poll_logits(split ? lane : threadIdx.x, split ? 32 : LW * 32);
+        if (split) __syncwarp();
+        else cbar();
+        for (int t = warp; t < a.T; t += LW) topk_token(t);
         cbar();
         group();
     }
@@ -1124,7 +1200,7 @@ struct LayerKernel {
     // (token, slot) pairs grouped by owned expert, ascending ids, tokens
     // ascending; built by warp 0 alone (warp-synchronous, no block barriers)
     __device__ void group() {
-        if (a.T == 1 && warp == 0) {
+        if (NT == 1 && warp == 0) {   // NT == 1: the launch has one token
             // one token: the k ids are distinct, each expert has one pair; the
             // unique list is the owned ids in ascending order
             const moe_expert *T = table();
@@ -1145,7 +1221,7 @@ struct LayerKernel {
                 plist()[rank] = lane;
             }
             if (lane == 0) { uoff()[U] = U; m->U = U; }
-        } else if (warp == 0) {
+        } else if (NT != 1 && warp == 0) {
             const int nw = (a.E + 31) >> 5;
             m->bitmap[lane] = 0u;   // MOE_MAX_EXPERTS / 32 == 32 words
             __syncwarp();
@@ -1213,36 +1289,20 @@ struct LayerKernel {
     // unit counts and this block's B range: every block's A bytes follow from
     // the snake deal; block c gets the B units whose byte midpoints fall in
     // its share of what is left to reach the mean (integer bytes throughout,
-    // so every block computes the same boundaries)
+    // so every block computes the same boundaries).  B ranges are contiguous,
+    // so a block's B units need the h of one or two experts.  The blocks that
+    // run the last A pass (one unit more than the rest) take the B units at
+    // the end of the list, whose experts' h that pass completes; the others
+    // take the experts finished by earlier passes, which their own earlier
+    // finish lets them start at once.  So the B order over blocks runs
+    // backwards when the last pass is a forward one.
     __device__ void plan() {
-        typedef unsigned long long u64;
+        // bytes in 128-byte lines (every packed tile is a whole number of
+        // them), so all of it is 32-bit integer arithmetic: the host refuses
+        // shapes whose layer could reach 2^31 lines
+        const uint32_t sa = 2u * (uint32_t)(FS::tile_bytes(a.H) >> 7), ra = 2u * (uint32_t)(F::tile_bytes(a.H) >> 7);
+        const uint32_t sb = a.shared ? (uint32_t)(FS::tile_bytes(a.Is) >> 7) : 0u, rb = (uint32_t)(F::tile_bytes(a.I) >> 7);
         const int tid = threadIdx.x;
-        if (a.T == 1) {
-            // one snake over A units then B units: B units of a block belong to
-            // different experts, but every expert has a single pair, so one hq
-            // batch holds them all
-            if (tid == 0) {
-                m->tilesI = a.I / 32;
-                m->tilesIs = a.shared ? a.Is / 32 : 0;
-                m->tilesH = a.H / 32;
-                m->n_ra = m->U * m->tilesI;
-                m->nA = m->n_sa + m->n_ra;
-                m->n_sb = a.shared ? m->tilesH : 0;
-                m->n_rb = m->U * m->tilesH;
-                m->nB = m->n_sb + m->n_rb;
-                m->bsnake = 1;
-                int pass = 0;
-                while (snake_unit(pass, c, G) < m->nA) ++pass;
-                m->bp0 = pass;
-                int n = 0;
-                while (snake_unit(pass + n, c, G) < m->nA + m->nB) ++n;
-                m->nb = n;
-            }
-            cbar();
-            return;
-        }
-        const u64 sa = 2ull * FS::tile_bytes(a.H), ra = 2ull * F::tile_bytes(a.H);
-        const u64 sb = a.shared ? (u64)FS::tile_bytes(a.Is) : 0ull, rb = (u64)F::tile_bytes(a.I);
         if (tid == 0) {
             m->tilesI = a.I / 32;
             m->tilesIs = a.shared ? a.Is / 32 : 0;
@@ -1252,64 +1312,101 @@ struct LayerKernel {
             m->n_sb = a.shared ? m->tilesH : 0;
             m->n_rb = m->U * m->tilesH;
             m->nB = m->n_sb + m->n_rb;
-            const u64 tot = (u64)m->n_sa * sa + (u64)m->n_ra * ra + (u64)m->n_sb * sb + (u64)m->n_rb * rb;
-            m->target = (u64)((float)tot / (float)G) + 1ull;   // any fixed rule works: all blocks agree
-        }
-        cbar();
-        u64 my_a = 0;
-        if (tid < G) {
-            for (int pass = 0; pass * G < m->nA; ++pass) {
-                const int j = snake_unit(pass, tid, G);
-                if (j < m->n_sa) my_a += sa;
-                else if (j < m->nA) my_a += ra;
+            const uint32_t tot = (uint32_t)m->n_sa * sa + (uint32_t)m->n_ra * ra + (uint32_t)m->n_sb * sb +
+                                 (uint32_t)m->n_rb * rb;
+            const uint32_t target = tot / (uint32_t)G + 1u;   // any fixed rule works: all blocks agree
+            m->target = target;
+            // no block's A bytes exceed the mean: the shares need no clamping,
+            // and block c's share starts at c * target - (A bytes of blocks < c)
+            const int npass = (m->nA + G - 1) / G;
+            const uint32_t amax = (uint32_t)npass * (sa > ra ? sa : ra);
+            m->brev = npass > 0 && ((npass - 1) & 1) == 0;
+            m->closed = amax <= target;
+            if (m->closed) {
+                if (m->brev) {   // B order G-1, ..., 0: the blocks above c come first
+                    const uint32_t atot = a_before(G, sa, ra);
+                    m->lo = (uint32_t)(G - 1 - c) * target - (atot - a_before(c + 1, sa, ra));
+                    m->hi = (uint32_t)(G - c) * target - (atot - a_before(c, sa, ra));
+                } else {
+                    m->lo = (uint32_t)c * target - a_before(c, sa, ra);
+                    m->hi = (uint32_t)(c + 1) * target - a_before(c + 1, sa, ra);
+                }
             }
         }
-        const u64 b = (tid < G && m->target > my_a) ? m->target - my_a : 0ull;
-        u64 inc = b;
+        cbar();
+        if (!m->closed) {   // a block-wide scan of the clamped shares
+            uint32_t my_a = 0;
+            const int bc = m->brev ? G - 1 - tid : tid;   // the block at B position tid
+            if (tid < G) {
+                for (int pass = 0; pass * G < m->nA; ++pass) {
+                    const int j = snake_unit(pass, bc, G);
+                    if (j < m->n_sa) my_a += sa;
+                    else if (j < m->nA) my_a += ra;
+                }
+            }
+            const uint32_t b = (tid < G && m->target > my_a) ? m->target - my_a : 0u;
+            uint32_t inc = b;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const u64 v = __shfl_up_sync(0xFFFFFFFFu, inc, off);
-            if (lane >= off) inc += v;
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, inc, off);
+                if (lane >= off) inc += v;
+            }
+            if (lane == 31) m->bsum[warp] = inc;
+            cbar();
+            uint32_t before = 0;
+            for (int w = 0; w < warp; ++w) before += m->bsum[w];
+            const uint32_t excl = before + inc - b;
+            const int pos = m->brev ? G - 1 - c : c;   // this block's B position
+            if (tid == pos) m->lo = excl;
+            if (tid == pos + 1) m->hi = excl;
+            cbar();
         }
-        if (lane == 31) m->bsum[warp] = inc;
-        cbar();
-        u64 before = 0;
-        for (int w = 0; w < warp; ++w) before += m->bsum[w];
-        const u64 excl = before + inc - b;
-        if (tid == c) m->lo = excl;
-        if (tid == c + 1) m->hi = excl;
-        cbar();
         if (tid == 0) {
+            const bool last = m->brev ? c == 0 : c + 1 == G;   // last in B order
             m->jb0 = first_b_unit(m->lo, sb, rb);
-            m->jb1 = (c + 1 == G) ? m->nB : first_b_unit(m->hi, sb, rb);
+            m->jb1 = last ? m->nB : first_b_unit(m->hi, sb, rb);
             if (m->jb1 < m->jb0) m->jb1 = m->jb0;
-            m->bsnake = 0;
             m->nb = m->jb1 - m->jb0;
         }
         cbar();
     }
 
-    // the n-th B unit of this block (global unit index)
-    __device__ int b_unit(int n) {
-        return p.bsnake ? snake_unit(p.bp0 + n, c, G) : p.nA + p.jb0 + n;
+    // A lines of blocks [0, c) under the snake deal: pass p gives them units
+    // [pG, pG + c) (even p) or [pG + G - c, pG + G) (odd p); units below
+    // n_sa are shared-expert units of sa lines, the rest up to nA routed of ra
+    __device__ uint32_t a_before(int cc, uint32_t sa, uint32_t ra) {
+        const int n_sa = m->n_sa, nA = m->nA;
+        auto span = [](int lo, int hi, int a0, int a1) -> uint32_t {
+            const int l = lo > a0 ? lo : a0, h = hi < a1 ? hi : a1;
+            return h > l ? (uint32_t)(h - l) : 0u;
+        };
+        uint32_t s = 0;
+        for (int p = 0; p * G < nA; ++p) {
+            const int lo = (p & 1) ? p * G + G - cc : p * G;
+            s += sa * span(lo, lo + cc, 0, n_sa) + ra * span(lo, lo + cc, n_sa, nA);
+        }
+        return s;
     }
 
-    // first B unit whose byte midpoint is >= X (B list: shared units of sb
-    // bytes, then routed units of rb bytes)
-    __device__ int first_b_unit(unsigned long long X, unsigned long long sb, unsigned long long rb) {
-        typedef unsigned long long u64;
+    // the n-th B unit of this block (global unit index)
+    __device__ int b_unit(int n) {
+        return p.nA + p.jb0 + n;
+    }
+
+    // first B unit whose midpoint is >= X (B list: shared units of sb lines,
+    // then routed units of rb lines; midpoints in half lines)
+    __device__ int first_b_unit(uint32_t X, uint32_t sb, uint32_t rb) {
         const int n_sb = m->n_sb, nB = m->nB;
-        auto mid = [&](int j) -> u64 {
-            return j < n_sb ? (u64)j * sb + sb / 2 : (u64)n_sb * sb + (u64)(j - n_sb) * rb + rb / 2;
+        const uint32_t X2 = 2u * X;
+        auto mid2 = [&](int j) -> uint32_t {
+            return j < n_sb ? (2u * (uint32_t)j + 1u) * sb : 2u * (uint32_t)n_sb * sb + (2u * (uint32_t)(j - n_sb) + 1u) * rb;
         };
-        // fp32 estimate, then exact integer correction
         int j;
-        if (n_sb > 0 && X <= mid(n_sb - 1)) j = (int)((float)X / (float)sb);
-        else j = n_sb + (int)((float)(X > (u64)n_sb * sb ? X - (u64)n_sb * sb : 0ull) / (float)rb);
+        if (n_sb > 0 && X2 <= mid2(n_sb - 1)) j = (int)(X / sb);
+        else j = n_sb + (int)((X > (uint32_t)n_sb * sb ? X - (uint32_t)n_sb * sb : 0u) / rb);
         if (j > nB) j = nB;
-        if (j < 0) j = 0;
-        while (j < nB && mid(j) < X) ++j;
-        while (j > 0 && mid(j - 1) >= X) --j;
+        while (j < nB && mid2(j) < X2) ++j;
+        while (j > 0 && mid2(j - 1) >= X2) --j;
         return j;
     }
 
@@ -1333,7 +1430,7 @@ struct LayerKernel {
     }
 
     __device__ void producer() {
-        Ring R{0, 0, 0};
+        Ring R{0, 0, 0, evict_first_policy()};
         if (lane == 0) {
             // input-independent bytes: router rows, expert table, shared gate/up
             int e0, e1;
@@ -1343,13 +1440,32 @@ struct LayerKernel {
             const uint32_t tb = a.table_in_smem ? (uint32_t)(a.E * sizeof(moe_expert)) : 0u;
             if (rbytes + tb > 0) {
                 mbar_arm(fixed_bar(), rbytes + tb);
-                if (rbytes) bulk_g2s(sm + o.router, (const uint8_t *)a.w_router + (size_t)e0 * rowb, rbytes, fixed_bar());
+                if (rbytes)
+                    bulk_g2s_stream(sm + o.router, (const uint8_t *)a.w_router + (size_t)e0 * rowb, rbytes, fixed_bar(),
+                                    R.pol);
                 if (tb) bulk_g2s(sm + o.table, a.experts, tb, fixed_bar());
             }
-            for (int pass = 0; !m->abort; ++pass) {
-                const int j = snake_unit(pass, c, G);
-                if (pass * G >= p.n_sa) break;
-                if (j < p.n_sa && !issue_unit(R, j)) break;
+        }
+        // This block's shared-expert units come first in its snake passes.
+        // Their items go out now as far as the empty ring holds them: the
+        // consumers take them only after the routing, so nothing is reclaimed
+        // before the handoff, and a request that had to wait for room would
+        // never be served.  (spass, sq): the first item not yet requested.
+        int spass = 0, sq = 0;
+        if (lane == 0) {
+            for (; spass * G < p.n_sa && !m->abort; ++spass, sq = 0) {
+                const int j = snake_unit(spass, c, G);
+                if (j >= p.n_sa) break;   // later passes hold routed units only
+                Unit U;
+                unit_of(j, U);
+                for (; sq < U.nitems; ++sq) {
+                    int r0, r1;
+                    item_recs(U, sq, r0, r1);
+                    const uint32_t run = run_bytes(U, r0, r1);
+                    if (R.issued >= NBAR || R.head + 2 * run > a.ring_bytes) break;
+                    issue(R, U, sq);
+                }
+                if (sq < U.nitems) break;
             }
         }
         if (lane == 0 && a.shared) m->shx = *a.shared;   // for units after the handoff
@@ -1357,10 +1473,11 @@ struct LayerKernel {
         shp = &m->shx;
         load_plan();
         if (lane == 0 && !m->abort) {
-            for (int pass = 0;; ++pass) {
+            // the remaining shared-expert items, then the routed units
+            for (int pass = spass; pass * G < p.nA; ++pass) {
                 const int j = snake_unit(pass, c, G);
-                if (pass * G >= p.nA) break;
-                if (j >= p.n_sa && j < p.nA && !issue_unit(R, j)) break;
+                if (j >= p.nA) continue;
+                if (!issue_unit(R, j, pass == spass ? sq : 0)) break;
             }
             for (int n = 0; n < p.nb && !m->abort; ++n)
                 if (!issue_unit(R, b_unit(n))) break;
@@ -1374,45 +1491,36 @@ struct LayerKernel {
 
     __device__ void consumer() {
         pdl_wait();
-        if (threadIdx.x == 0) m->ep = ld_relaxed_u32(a.epoch) + 1u;
+        if (threadIdx.x == 0) {
+            m->ep = ld_relaxed_u32(a.epoch) + 1u;
+            arrived = count_epoch_read(a.arrive);
+        }
         // an fp32 router needs only x: its logits go out first and x is
         // quantised while the other blocks publish theirs; a Q8_0 router dots
         // the quantised x
         const bool xq_first = a.rtype == MOE_Q8_0;
-        if (xq_first) quantise_x();
+        if (xq_first) quantise_x(0);
         cbar();
         ep = m->ep;
         router_logits();
-        if (!xq_first) {
-            quantise_x();
-            cbar();
-        }
+        route_tail(xq_first);
         if (c == 0 && a.xq_out) {
             const int n16 = (int)(a.xrec / 16);
             for (int i = threadIdx.x; i < a.T * n16; i += LW * 32)
                 reinterpret_cast<uint4 *>(a.xq_out)[i] = reinterpret_cast<const uint4 *>(sm + o.xq)[i];
         }
-        // shared-expert gate/up while the other blocks publish their logits
-        int item = 0, rbuf = 0;
-        for (int pass = 0;; ++pass) {
-            const int j = snake_unit(pass, c, G);
-            if (pass * G >= p.n_sa) break;
-            if (j < p.n_sa) {
-                Unit U;
-                unit_of(j, U);
-                run_A<FS>(U, item, rbuf);
-            }
-        }
-        topk_and_group();
         bar_handoff();
         gating_weights();
-        for (int pass = 0;; ++pass) {
+        // A units in ring order: this block's shared-expert units (their
+        // records were requested before the routing), then its routed ones
+        int item = 0, ua = 0;
+        for (int pass = 0; pass * G < p.nA; ++pass) {
             const int j = snake_unit(pass, c, G);
-            if (pass * G >= p.nA) break;
-            if (j >= p.n_sa && j < p.nA) {
+            if (j < p.nA) {
                 Unit U;
                 unit_of(j, U);
-                run_A<F>(U, item, rbuf);
+                if (std::is_same<F, FS>::value || j >= p.n_sa) run_A<F>(U, item, ua);
+                else run_A<FS>(U, item, ua);
             }
         }
         // no loop below leaves early: every consumer thread must reach every
@@ -1427,16 +1535,18 @@ struct LayerKernel {
         shp = &m->shx;
     }
 
-    // block 0 advances the epoch once it is done: every block read it before
-    // publishing its logits, which block 0 has consumed; the next launch reads
-    // it after this grid has completed
     __device__ void finish() {
-        if (c == 0 && threadIdx.x == 0) st_relaxed_u32(a.epoch, m->ep);
+        if (threadIdx.x == 0 && arrived + 1u == (uint32_t)G) {
+            st_relaxed_u32(a.arrive, 0u);
+            st_relaxed_u32(a.epoch, m->ep);
+        }
     }
 };
 
+// one block per SM: the whole register file is the block's (17 warps: five
+// share one SM sub-partition's 16K registers, so 96 per thread; 9 warps: 224)
 template <class F, class FS, int NT>
-__global__ void __launch_bounds__(LT, 1) layer_kernel(const __grid_constant__ LayerArgs a) {
+__global__ void __launch_bounds__(Warps<NT>::LT, 1) layer_kernel(const __grid_constant__ LayerArgs a) {
     LayerKernel<F, FS, NT> K(a, moe_smem);
     K.run();
 }
@@ -1451,16 +1561,21 @@ cudaError_t launch_layer_t(const LayerArgs &a, int G, size_t smem, bool pdl, cud
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64 && occ_ok[dev] < (int)smem + 1) {
         int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, layer_kernel<F, FS, NT>, LT, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, layer_kernel<F, FS, NT>, Warps<NT>::LT, smem);
         if (e != cudaSuccess) return e;
-        if (n < 1) return cudaErrorInvalidConfiguration;   // every block must be resident at once
+        if (n < 1) return cudaErrorInvalidConfiguration;   // one block per SM must fit
         occ_ok[dev] = (int)smem + 1;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)G);
-    cfg.blockDim = dim3(LT);
+    cfg.blockDim = dim3(Warps<NT>::LT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
+    // Not a cooperative launch: with that attribute a launch starts only once
+    // the previous kernel has left every SM, which undoes the overlap below.
+    // Co-residency of the blocks is assumed (one block per SM fits, checked
+    // above); a block kept off its SM by other work makes the others' waits
+    // run into their bound (MOE_DEV_TIMEOUT), it does not hang.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;

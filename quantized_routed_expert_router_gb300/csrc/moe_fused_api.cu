@@ -11,7 +11,9 @@ cudaError_t launch_layer_q80(const LayerArgs &a, int sqtype, int G, size_t smem,
 cudaError_t launch_layer_mx4(const LayerArgs &a, int sqtype, int G, size_t smem, bool pdl, cudaStream_t s);
 
 // constants mirrored from moe_fused.cuh (kept in one place there; checked below)
-constexpr int kLW = 8, kNBAR = 32;
+constexpr int kNBAR = 32;
+// consumer warps of the kernel for a launch's token count (Warps<NT> in the kernel)
+static int consumer_warps(int NT) { return NT == 1 ? 16 : 8; }
 constexpr uint32_t kRingDefault = 160 * 1024;
 
 static size_t al16(size_t v) { return (v + 15) & ~(size_t)15; }
@@ -22,6 +24,7 @@ LayerWs layer_ws_layout(int T, int k, int H, int I, int Is, int E) {
     LayerWs w;
     w.status = 0;
     w.epoch = 64;
+    w.arrive = 128;
     w.logits = 256;
     w.h_r = al(w.logits + 8 * (size_t)T * E);
     w.h_s = al(w.h_r + 8 * P * I);
@@ -43,6 +46,24 @@ static uint32_t max_rec(int q, int cols) {
         }
     }
 }
+static size_t tile_bytes_of(int q, int cols) {
+    switch (q) {
+        case MOE_Q4_K: return FQ4K::tile_bytes(cols);
+        case MOE_Q2_K: return FQ2K::tile_bytes(cols);
+        case MOE_Q8_0: return FQ80::tile_bytes(cols);
+        default: return FMX4::tile_bytes(cols);
+    }
+}
+
+// The kernel's work plan counts bytes in 128-byte lines with 32-bit
+// integers: every expert of the call at once must stay below 2^30 lines.
+static bool plan_fits(const LayerArgs &a, int qtype, int sqtype) {
+    const size_t P = (size_t)a.T * a.k;
+    size_t lines = P * (2 * tile_bytes_of(qtype, a.H) * (size_t)(a.I / 32) + tile_bytes_of(qtype, a.I) * (size_t)(a.H / 32));
+    if (a.shared) lines += 2 * tile_bytes_of(sqtype, a.H) * (size_t)(a.Is / 32) + tile_bytes_of(sqtype, a.Is) * (size_t)(a.H / 32);
+    return (lines >> 7) < ((size_t)1 << 30);
+}
+
 // smallest possible ring item of a format: a gate+up record pair, or one down record
 static uint32_t max_item(int q, int H, int I) {
     const uint32_t a = 2 * max_rec(q, H), b = max_rec(q, I);
@@ -56,6 +77,7 @@ static int lg_recs_per_item(size_t ring, uint32_t rec_bytes) {
 }
 
 cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStream_t s) {
+    if (!plan_fits(a, qtype, sqtype)) return cudaErrorNotSupported;
     int G = num_sms();
     if (G > 256) G = 256;
     const int nseg = (a.H + 1023) / 1024;
@@ -71,7 +93,11 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
     const int Imax = a.Is > a.I ? a.Is : a.I;
     a.hrec = q8_row_bytes(Imax);
     a.NT = a.T <= 1 ? 1 : 4;   // batches above 4 tokens never reach the fused kernel
-    const size_t red_bytes = (size_t)(a.NT <= 4 ? 2 : 1) * kLW * 2 * a.NT * 32 * 4;
+    // A units: two alternating buffers of the warps' gate and up partials;
+    // B batches: per-record partials, 64 slots for one token, 32 for four
+    a.bslots = a.NT == 1 ? 64 : 32;
+    size_t red_bytes = (size_t)2 * consumer_warps(a.NT) * 2 * a.NT * 32 * 4;
+    if ((size_t)a.bslots * a.NT * 32 * 4 > red_bytes) red_bytes = (size_t)a.bslots * a.NT * 32 * 4;
 
     Smem o;
     size_t off = 0;
@@ -82,7 +108,7 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
     };
     const size_t fixed_router = (size_t)rr * rowb;
     // everything but the ring and the hq records
-    const size_t fixed_core = (2 * kNBAR + 1) * 8 + 2 * kNBAR * 4 + fixed_router +
+    const size_t fixed_core = (2 * kNBAR + 5) * 8 + 2 * kNBAR * 4 + fixed_router +
                               (a.table_in_smem ? a.E * sizeof(moe_expert) : 0) + a.T * a.xrec +
                               4 * (size_t)a.T * a.E + 4 * (size_t)rr * nseg * a.T + 8 * (size_t)a.P +
                               4 * (5 * (size_t)a.P + 1) + red_bytes + kLayerMiscBytes + 16 * 16;
@@ -115,7 +141,7 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
         a.lgrb = lg_recs_per_item(ring, pb);
     }
     o.ring = take(ring);
-    o.bars = take((2 * kNBAR + 1) * 8);
+    o.bars = take((2 * kNBAR + 5) * 8);   // ring full/empty, fixed bytes, A partials ready/free x 2
     o.starts = take(2 * kNBAR * 4);   // item start offsets, then slot tags
     o.router = take(fixed_router);
     o.table = take(a.table_in_smem ? a.E * sizeof(moe_expert) : 0);
@@ -233,6 +259,7 @@ moe_status moe_layer_forward(const float *hidden, int T, const void *w_router, m
     a.xq_out = (uint8_t *)xq_out;
     a.status = (unsigned *)(w + L.status);
     a.epoch = (unsigned *)(w + L.epoch);
+    a.arrive = (unsigned *)(w + L.arrive);
     typedef unsigned long long tw;
     a.logits = (tw *)(w + L.logits);
     a.h_r = (tw *)(w + L.h_r);

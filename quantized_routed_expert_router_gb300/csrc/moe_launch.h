@@ -59,7 +59,7 @@ struct LayerArgs {
     float *w_out;
     float *logits_out;
     uint8_t *xq_out;
-    unsigned *status, *epoch;       // workspace: status word, launch counter
+    unsigned *status, *epoch, *arrive;   // workspace: status word, launch counter, epoch readers
     // tagged words (value bits | epoch << 32): logits [T][E], h [T*k][I],
     // shared h [T][Is], o [T*k][H], shared o [T][H]
     unsigned long long *logits, *h_r, *h_s, *o_r, *o_s;
@@ -67,6 +67,7 @@ struct LayerArgs {
     int T, H, I, Is, E, P, NT;
     int table_in_smem;
     int hq_slots;                   // q8 records of requantised h the block can hold
+    int bslots;                     // B-record partial-sum slots of the reduction buffer
     uint32_t ring_bytes;
     int lgra, lgrb;                 // log2 of the records per ring item: A (gate + up runs), B (down run)
     size_t xrec, hrec;
@@ -74,11 +75,16 @@ struct LayerArgs {
 };
 
 struct LayerWs {
-    size_t status, epoch, logits, h_r, h_s, o_r, o_s, total;
+    size_t status, epoch, arrive, logits, h_r, h_s, o_r, o_s, total;
 };
 LayerWs layer_ws_layout(int T, int k, int H, int I, int Is, int E);
 // plans shared memory and launches the fused layer kernel for the pool's formats
 cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStream_t s);
+
+// every argument check of moe_expert_ffn except the workspace's (MOE_OK for
+// T == 0 once the shapes are valid)
+moe_status ffn_check_args(const void *xq, int T, const int32_t *ids, const float *weights, int k,
+                          const moe_pool *pool, const moe_pool *shared, const float *y);
 
 // workspace layout of moe_expert_ffn (offsets in bytes)
 struct FfnWs {

@@ -51,11 +51,10 @@ using namespace moe;
 extern "C" moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, const float *weights,
                                              int k, const moe_pool *pool, const moe_pool *shared, float *y,
                                              cudaStream_t stream) {
-    if (T < 0 || T > MOE_MAX_TOKENS || k < 1 || k > MOE_MAX_K) return MOE_ERR_INVALID_ARG;
-    if (!pool || !pool->experts || pool->E < 1 || pool->E > MOE_MAX_EXPERTS) return MOE_ERR_INVALID_ARG;
-    if (pool->H <= 0 || pool->I <= 0 || pool->H % 32 || pool->I % 32) return MOE_ERR_INVALID_ARG;
-    if (shared && (!shared->experts || shared->E != 1 || shared->I <= 0 || shared->I % 32))
-        return MOE_ERR_INVALID_ARG;
+    // every check moe_expert_ffn makes comes first, so a call it would reject
+    // enqueues nothing (not even the clear of the shared scratch below)
+    const moe_status v = ffn_check_args(xq, T, ids, weights, k, pool, shared, y);
+    if (v != MOE_OK) return v;
     const FfnWs L = ffn_ws_layout(T, k, pool->H, pool->I, shared ? shared->I : 0);
     if (L.total > kStaticScratchBytes) return MOE_ERR_WORKSPACE;   // beyond the fixed scratch
     if (T == 0) return MOE_OK;

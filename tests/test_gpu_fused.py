@@ -54,8 +54,10 @@ def test_fused_layer_parity(name, flags):
         for g, w in zip(unpack_q8_records(np_(dl.xq), T, cfg.H), ref["xq"]):
             assert np.array_equal(g, w)
         assert_y_close(np_(dl.y), ref["y"], name)
-        # same arithmetic and summation order as the three calls
-        assert np.array_equal(np_(dl.y), y3), rep
+        if T > 1:   # same arithmetic and summation order as the three calls
+            assert np.array_equal(np_(dl.y), y3), rep
+        else:       # one token: a unit's gate/up records are dealt over 16 warps
+            assert_y_close(np_(dl.y), y3.astype(np.float64), name)   # (8 in the three calls)
 
 
 def test_fused_ownership_partition():

@@ -448,7 +448,25 @@ SMALL = {
                                 qtype=synth.Q6_K, shared_qtype=synth.Q6_K),
     "q3_K+q8_0shared": synth.shrink(synth.CONFIGS["wide"], H=512, I=256, E=8, k=3, shared_I=256,
                                     qtype=synth.Q3_K),
+    # x in 256-blocks, h in 32-blocks: a slip that used H's block for h fails here
+    "q8_0 H512/I288": synth.shrink(synth.CONFIGS["tiny"], H=512, I=288, E=6, k=2),
 }
+
+
+def np_quantize(x):
+    """The activation rule restated in numpy fp32 (IEEE division, round half
+    to even): per block of B (256, else 32), d = amax/127 and
+    q = rint(x * (127/amax)); zero blocks give d = 0, q = 0."""
+    x = np.asarray(x, np.float32)
+    n = x.shape[-1]
+    B = 256 if n % 256 == 0 else 32
+    xb = x.reshape(-1, n // B, B)
+    amax = np.abs(xb).max(axis=-1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        d = np.where(amax > 0, amax / np.float32(127), np.float32(0)).astype(np.float32)
+        isc = np.where(amax > 0, np.float32(127) / amax, np.float32(0)).astype(np.float32)
+    q = np.clip(np.rint((xb * isc[..., None]).astype(np.float32)), -127, 127).astype(np.int8)
+    return d.reshape(x.shape[:-1] + (n // B,)), q.reshape(x.shape)
 
 
 @pytest.mark.parametrize("name", list(SMALL))
@@ -466,6 +484,11 @@ def test_ffn_matches_fp64_brute_force(name):
             h64 = (brute.silu(g) * u)[0]
             h32 = res["h"][t, s].astype(np.float64)
             assert np.all(np.abs(h32 - h64) <= 2.0 ** -23 * np.abs(h64) + 1e-30)
+            # the routed h goes into the down projection requantised with the
+            # activation rule at I's own block size
+            d_np, q_np = np_quantize(res["h"][t, s])
+            assert np.array_equal(np.asarray(res["hd"][t, s], np.float32).reshape(-1), d_np.reshape(-1))
+            assert np.array_equal(np.asarray(res["hq"][t, s]).reshape(-1), q_np.reshape(-1))
     hq_sh = None
     if cfg.has_shared:
         g, u = brute.expert_gu(L, 0, xv, shared=True)

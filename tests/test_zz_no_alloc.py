@@ -44,9 +44,20 @@ def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
+    """Real (small) device buffers: the call must refuse the shape before it
+    enqueues anything, so y keeps its NaNs."""
     L = moe.lib()
-    pool = moe._Pool(moe.Q4_K, 4096, 4096, 256, 1 << 20)
+    T, k, H, I, E = 16, 32, 4096, 4096, 256
+    dev = "cuda"
+    xq = torch.zeros(T * moe.moe_q8_row_bytes(H), dtype=torch.uint8, device=dev)
+    ids = torch.zeros((T, k), dtype=torch.int32, device=dev)
+    w = torch.zeros((T, k), dtype=torch.float32, device=dev)
+    y = torch.full((T, H), float("nan"), device=dev)
+    table = torch.zeros((E, 6), dtype=torch.int64, device=dev)   # every expert "not mine"
+    pool = moe._Pool(moe.Q4_K, H, I, E, table.data_ptr())
     # T=16, k=32, I=4096: the h scratch alone is 8 MiB > 2 MiB
-    rc = L.moe_expert_ffn_noalloc(1 << 20, 16, 1 << 20, 1 << 20, 32, ctypes.byref(pool), None, 1 << 20,
-                                  ctypes.c_void_p(0))
+    rc = L.moe_expert_ffn_noalloc(xq.data_ptr(), T, ids.data_ptr(), w.data_ptr(), k, ctypes.byref(pool), None,
+                                  y.data_ptr(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == 3, moe.status_str(rc)
+    torch.cuda.synchronize()
+    assert bool(torch.isnan(y).all())
