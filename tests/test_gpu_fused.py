@@ -125,3 +125,24 @@ def test_fused_stack_replayed_from_a_cuda_graph():
         for L, dl, ref in zip(layers, dls, refs):
             assert moe.moe_read_device_status(dl.ws_layer) == 0
             assert_y_close(np_(dl.y), ref, f"replay {rep}, layer {L.layer}")
+
+
+@pytest.mark.parametrize("T", [1, 3])
+@pytest.mark.parametrize("E,k", [(64, 6), (256, 8), (64, 2)])
+def test_fused_topk_ties_take_the_lowest_index(T, E, k):
+    """Router rows repeated in groups of 8 give exactly equal logits: the
+    one-launch selection must keep the k largest with the lower expert index
+    first on ties, as the oracle does."""
+    cfg = synth.shrink(synth.CONFIGS["a3b"], H=512, I=256, E=E, k=k, shared_I=0)
+    L = synth.make_layer(cfg, 0, T=T)
+    base = synth.normal(6, 1, 0.02, E // 8, cfg.H)
+    L.router = np.ascontiguousarray(np.repeat(base, 8, axis=0))
+    ref = oracle.layer_forward(L)
+    assert len(np.unique(ref["logits"][0])) < E          # ties are present
+    dl = DeviceLayer(L, "cuda")
+    dl.forward_fused()
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(dl.ws_layer) == 0
+    assert np.array_equal(np_(dl.logits), ref["logits"])
+    assert np.array_equal(np_(dl.ids), ref["ids"])
+    assert_y_close(np_(dl.y), ref["y"], f"ties E{E} k{k} T{T}")
