@@ -57,7 +57,9 @@ typedef enum {
     MOE_Q8_0 = 1,   /* 32 weights: f16 d, i8 q[32]               w = d*q   (34 B)  */
     MOE_Q4_K = 2,   /* 256 weights: f16 d, f16 dmin, 6-bit sc/m x 8, 4-bit q (144 B) */
     MOE_Q2_K = 3,   /* 256 weights: 4-bit sc/m x 16, 2-bit q, f16 d, f16 dmin (84 B) */
-    MOE_MXFP4 = 4   /* 32 weights: E8M0 scale e, FP4 E2M1 q[32]  w = 2^(e-127)*q (17 B) */
+    MOE_MXFP4 = 4,  /* 32 weights: E8M0 scale e, FP4 E2M1 q[32]  w = 2^(e-127)*q (17 B) */
+    MOE_Q6_K = 5,   /* 256 weights: 4+2-bit q (offset 32), i8 sc x 16, f16 d     (210 B) */
+    MOE_Q3_K = 6    /* 256 weights: 2+1-bit q (offset 4), 6-bit sc x 16, f16 d   (110 B) */
 } moe_qtype;
 
 typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID = 1 } moe_gating;
@@ -88,9 +90,11 @@ int moe_act_block(int n);
 size_t moe_q8_row_bytes(int n);
 
 /* Bytes of a packed weight matrix (rows x cols), 0 if unsupported.
- * rows % 32 == 0; cols % 256 == 0 for Q4_K, Q2_K and Q8_0; cols % 32 == 0 for
- * MXFP4.  The packed size equals the GGUF size except for MXFP4 matrices whose
- * cols/32 is not a multiple of 8 (a few pad bytes per 32 rows). */
+ * rows % 32 == 0; cols % 256 == 0 for Q4_K, Q2_K, Q8_0, Q6_K and Q3_K;
+ * cols % 32 == 0 for MXFP4.  The packed size equals the GGUF size except for
+ * MXFP4 matrices whose cols/32 is not a multiple of 8, Q6_K (4 bytes per row
+ * and 256 columns for d instead of 2) and Q3_K (112 bytes per row and 256
+ * columns instead of 110). */
 size_t moe_packed_bytes(moe_qtype qtype, int rows, int cols);
 
 /* ------------------------------------------------------------- one-time pack */
@@ -115,6 +119,10 @@ size_t moe_packed_bytes(moe_qtype qtype, int rows, int cols);
  *   MXFP4 : record = nb <= 8 blocks (the last record of a row takes the
  *           remainder); planes 0..nb-1 = qs of block b, then a 256-byte
  *           plane of 8 scale bytes per row (unused bytes zero). nb*512+256 B
+ *   Q6_K  : record = 1 block; planes 0..12 = bytes [16p, 16p+16) (ql, qh,
+ *           the 16 int8 scales), then a 128-byte plane of {d, 0, 0}.  6784 B
+ *   Q3_K  : record = 1 block; planes 0..5 = hmask and qs, plane 6 = the
+ *           12 scale bytes, d and two zero bytes.                    3584 B
  * Errors: MOE_ERR_UNSUPPORTED for F32 or shapes outside the rules above.
  */
 moe_status moe_pack_weights(const void *blocks, moe_qtype qtype, int rows, int cols,

@@ -15,7 +15,7 @@ import torch
 
 from . import _build
 
-F32, Q8_0, Q4_K, Q2_K, MXFP4 = 0, 1, 2, 3, 4
+F32, Q8_0, Q4_K, Q2_K, MXFP4, Q6_K, Q3_K = 0, 1, 2, 3, 4, 5, 6
 SOFTMAX, SIGMOID = 0, 1
 DEV_BAD_ID, DEV_DUP_ID = 0x1, 0x2
 MAX_TOKENS, MAX_K, MAX_EXPERTS = 16, 32, 1024

@@ -16,7 +16,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 SO = os.path.join(PKG, "_moe.so")
 SOURCES = ["moe_api.cu", "moe_kernels.cu", "moe_ffn.cu", "moe_noalloc.cu", "moe_fused_api.cu",
-           "moe_fused_q4k.cu", "moe_fused_q2k.cu", "moe_fused_q80.cu", "moe_fused_mx4.cu"]
+           "moe_fused_q4k.cu", "moe_fused_q2k.cu", "moe_fused_q80.cu", "moe_fused_mx4.cu", "moe_fused_q6k.cu",
+           "moe_fused_q3k.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

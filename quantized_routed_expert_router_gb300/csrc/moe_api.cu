@@ -11,7 +11,9 @@ namespace {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-bool expert_format(int q) { return q == MOE_Q8_0 || q == MOE_Q4_K || q == MOE_Q2_K || q == MOE_MXFP4; }
+bool expert_format(int q) {
+    return q == MOE_Q8_0 || q == MOE_Q4_K || q == MOE_Q2_K || q == MOE_MXFP4 || q == MOE_Q6_K || q == MOE_Q3_K;
+}
 
 // columns a packed matrix of this format accepts
 bool cols_ok(int q, int cols) {
@@ -27,6 +29,8 @@ size_t packed_bytes(int q, int rows, int cols) {
         case MOE_Q4_K: tile = FQ4K::tile_bytes(cols); break;
         case MOE_Q2_K: tile = FQ2K::tile_bytes(cols); break;
         case MOE_Q8_0: tile = FQ80::tile_bytes(cols); break;
+        case MOE_Q6_K: tile = FQ6K::tile_bytes(cols); break;
+        case MOE_Q3_K: tile = FQ3K::tile_bytes(cols); break;
         default: tile = FMX4::tile_bytes(cols); break;
     }
     return (size_t)(rows / 32) * tile;

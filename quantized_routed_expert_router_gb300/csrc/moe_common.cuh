@@ -385,6 +385,153 @@ struct FMX4 {
     }
 };
 
+// ------------------------------------------------------------------ Q6_K
+// record = one 256-column block per row: planes 0..12 = the block's bytes
+// [16p, 16p+16) (0..7: ql, 8..11: qh, 12: the 16 int8 scales), then a
+// 128-byte plane with d (f16 and two zero bytes) per row.  Element
+// i = 128n + 32s + l has its low nibble in ql[64n + 32(s%2) + l] (the high
+// nibble for s >= 2) and its top two bits at bits 2s of qh[32n + l]; the
+// stored 6-bit code u is the weight code + 32.  With 16-sub-blocks j = i/16,
+// isum_j = dot(u, x) - 32 * bsum_j (the signed codes' exact dot).
+struct FQ6K {
+    static constexpr int QK = 256;
+    static constexpr int NSUB = 16;
+    static constexpr int REC = 13 * 512 + 128;
+    struct W { uint4 ql[8]; uint4 qh[4]; uint4 sc; uint32_t d; };
+    __host__ __device__ static int nrec(int cols) { return cols / 256; }
+    __host__ __device__ static size_t rec_off(int, int r) { return (size_t)r * REC; }
+    __host__ __device__ static size_t tile_bytes(int cols) { return (size_t)(cols / 256) * REC; }
+    __host__ __device__ static uint32_t rec_bytes(int, int) { return REC; }
+    __host__ __device__ static int rec_blocks(int, int) { return 8; }
+    __device__ static void load(W &w, const uint8_t *rec, int, int lane) {
+#pragma unroll
+        for (int p = 0; p < 8; ++p) w.ql[p] = ldg_stream(rec + p * 512 + lane * 16);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) w.qh[p] = ldg_stream(rec + (8 + p) * 512 + lane * 16);
+        w.sc = ldg_stream(rec + 12 * 512 + lane * 16);
+        w.d = ldg_stream32(rec + 13 * 512 + lane * 4);
+    }
+    __device__ static void load_s(W &w, const uint8_t *rec, int, int lane) {
+#pragma unroll
+        for (int p = 0; p < 8; ++p) w.ql[p] = lds_u4(rec + p * 512 + lane * 16);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) w.qh[p] = lds_u4(rec + (8 + p) * 512 + lane * 16);
+        w.sc = lds_u4(rec + 12 * 512 + lane * 16);
+        w.d = lds_u1(rec + 13 * 512 + lane * 4);
+    }
+    __device__ static uint32_t wd(const uint4 &v, int i) { return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w)); }
+    __device__ static void isums(const W &w, const Act &a, int k0, int, int *is) {
+        const int8_t *x = a.q + k0;
+        const int16_t *bs = a.bs + (k0 >> 4);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const int4 xa = lds128(x + 128 * n + 32 * s), xb = lds128(x + 128 * n + 32 * s + 16);
+                const uint32_t xw[8] = {(uint32_t)xa.x, (uint32_t)xa.y, (uint32_t)xa.z, (uint32_t)xa.w,
+                                        (uint32_t)xb.x, (uint32_t)xb.y, (uint32_t)xb.z, (uint32_t)xb.w};
+                int acc0 = 0, acc1 = 0;
+#pragma unroll
+                for (int wl = 0; wl < 8; ++wl) {
+                    const uint32_t q = wd(w.ql[4 * n + 2 * (s & 1) + (wl >> 2)], wl & 3);
+                    const uint32_t h = wd(w.qh[2 * n + (wl >> 2)], wl & 3);
+                    const uint32_t lo = (s >= 2 ? (q >> 4) : q) & 0x0F0F0F0Fu;
+                    const uint32_t u = lo | (((h >> (2 * s)) & 0x03030303u) << 4);
+                    if (wl < 4) acc0 = dp4a(u, xw[wl], acc0);
+                    else acc1 = dp4a(u, xw[wl], acc1);
+                }
+                const int j = 8 * n + 2 * s;
+                is[j] = acc0 - 32 * (int)bs[j];
+                is[j + 1] = acc1 - 32 * (int)bs[j + 1];
+            }
+        }
+    }
+    // d_x * d * sum_j sc_j is_j
+    __device__ static float combine(const W &w, const Act &a, int k0, int, const int *is) {
+        const uint32_t sw[4] = {w.sc.x, w.sc.y, w.sc.z, w.sc.w};
+        int P = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) P += (int)(int8_t)byte_of(sw[j >> 2], j & 3) * is[j];
+        const float d = h2f(w.d);
+        const float dx = a.d[k0 >> a.lgB];
+        return dx * (d * (float)P);
+    }
+};
+
+// ------------------------------------------------------------------ Q3_K
+// record = one 256-column block per row: planes 0..1 = hmask, 2..5 = qs,
+// plane 6 = the 12 scale bytes, d (f16) and two zero bytes.  Element
+// i = 128n + 32s + l takes two bits at bits 2s of qs[32n + l] and bit
+// 4n + s of hmask[l]; u = low + 4 * bit is the weight code + 4.  With
+// 16-sub-blocks j, isum_j = dot(u, x) - 4 * bsum_j.  Scale j: 6 bits, low
+// nibble in byte j (j < 8) or the high nibble of byte j - 8, top two bits at
+// bit 2(j/4) of byte 8 + j%4, offset by 32.
+struct FQ3K {
+    static constexpr int QK = 256;
+    static constexpr int NSUB = 16;
+    static constexpr int REC = 7 * 512;
+    struct W { uint4 hm[2]; uint4 qs[4]; uint4 sd; };
+    __host__ __device__ static int nrec(int cols) { return cols / 256; }
+    __host__ __device__ static size_t rec_off(int, int r) { return (size_t)r * REC; }
+    __host__ __device__ static size_t tile_bytes(int cols) { return (size_t)(cols / 256) * REC; }
+    __host__ __device__ static uint32_t rec_bytes(int, int) { return REC; }
+    __host__ __device__ static int rec_blocks(int, int) { return 8; }
+    __device__ static void load(W &w, const uint8_t *rec, int, int lane) {
+#pragma unroll
+        for (int p = 0; p < 2; ++p) w.hm[p] = ldg_stream(rec + p * 512 + lane * 16);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) w.qs[p] = ldg_stream(rec + (2 + p) * 512 + lane * 16);
+        w.sd = ldg_stream(rec + 6 * 512 + lane * 16);
+    }
+    __device__ static void load_s(W &w, const uint8_t *rec, int, int lane) {
+#pragma unroll
+        for (int p = 0; p < 2; ++p) w.hm[p] = lds_u4(rec + p * 512 + lane * 16);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) w.qs[p] = lds_u4(rec + (2 + p) * 512 + lane * 16);
+        w.sd = lds_u4(rec + 6 * 512 + lane * 16);
+    }
+    __device__ static void isums(const W &w, const Act &a, int k0, int, int *is) {
+        const int8_t *x = a.q + k0;
+        const int16_t *bs = a.bs + (k0 >> 4);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const int4 xa = lds128(x + 128 * n + 32 * s), xb = lds128(x + 128 * n + 32 * s + 16);
+                const uint32_t xw[8] = {(uint32_t)xa.x, (uint32_t)xa.y, (uint32_t)xa.z, (uint32_t)xa.w,
+                                        (uint32_t)xb.x, (uint32_t)xb.y, (uint32_t)xb.z, (uint32_t)xb.w};
+                int acc0 = 0, acc1 = 0;
+#pragma unroll
+                for (int wl = 0; wl < 8; ++wl) {
+                    const uint32_t q = FQ6K::wd(w.qs[2 * n + (wl >> 2)], wl & 3);
+                    const uint32_t h = FQ6K::wd(w.hm[wl >> 2], wl & 3);
+                    const uint32_t u = ((q >> (2 * s)) & 0x03030303u) | (((h >> (4 * n + s)) & 0x01010101u) << 2);
+                    if (wl < 4) acc0 = dp4a(u, xw[wl], acc0);
+                    else acc1 = dp4a(u, xw[wl], acc1);
+                }
+                const int j = 8 * n + 2 * s;
+                is[j] = acc0 - 4 * (int)bs[j];
+                is[j + 1] = acc1 - 4 * (int)bs[j + 1];
+            }
+        }
+    }
+    // d_x * d * sum_j (s_j - 32) is_j
+    __device__ static float combine(const W &w, const Act &a, int k0, int, const int *is) {
+        const uint32_t lo[2] = {w.sd.x, w.sd.y}, hi = w.sd.z;
+        int P = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const uint32_t b = byte_of(lo[(j & 7) >> 2], j & 3);
+            const int low = (int)(j < 8 ? (b & 15u) : (b >> 4));
+            const int high = (int)((byte_of(hi, j & 3) >> (2 * (j >> 2))) & 3u);
+            P += ((low | (high << 4)) - 32) * is[j];
+        }
+        const float d = h2f(w.sd.w);
+        const float dx = a.d[k0 >> a.lgB];
+        return dx * (d * (float)P);
+    }
+};
+
 // ------------------------------------------------------------ quantiser
 // Activation quantisation rule (pulsar README, "MoE resolve": activations
 // quantised to q8_0/q8_K before integer dots).  Per block of B = 256 (32 where

@@ -388,6 +388,10 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t s) {
     if (q == MOE_Q2_K && sq == MOE_Q8_0) return launch_ffn_t<FQ2K, FQ80>(a, s);
     if (q == MOE_MXFP4 && sq == MOE_MXFP4) return launch_ffn_t<FMX4, FMX4>(a, s);
     if (q == MOE_MXFP4 && sq == MOE_Q8_0) return launch_ffn_t<FMX4, FQ80>(a, s);
+    if (q == MOE_Q6_K && sq == MOE_Q6_K) return launch_ffn_t<FQ6K, FQ6K>(a, s);
+    if (q == MOE_Q6_K && sq == MOE_Q8_0) return launch_ffn_t<FQ6K, FQ80>(a, s);
+    if (q == MOE_Q3_K && sq == MOE_Q3_K) return launch_ffn_t<FQ3K, FQ3K>(a, s);
+    if (q == MOE_Q3_K && sq == MOE_Q8_0) return launch_ffn_t<FQ3K, FQ80>(a, s);
     return cudaErrorNotSupported;
 }
 

@@ -9,6 +9,8 @@ cudaError_t launch_layer_q4k(const LayerArgs &a, int sqtype, int G, size_t smem,
 cudaError_t launch_layer_q2k(const LayerArgs &a, int sqtype, int G, size_t smem, bool pdl, cudaStream_t s);
 cudaError_t launch_layer_q80(const LayerArgs &a, int sqtype, int G, size_t smem, bool pdl, cudaStream_t s);
 cudaError_t launch_layer_mx4(const LayerArgs &a, int sqtype, int G, size_t smem, bool pdl, cudaStream_t s);
+cudaError_t launch_layer_q6k(const LayerArgs &a, int sqtype, int G, size_t smem, bool pdl, cudaStream_t s);
+cudaError_t launch_layer_q3k(const LayerArgs &a, int sqtype, int G, size_t smem, bool pdl, cudaStream_t s);
 
 // constants mirrored from moe_fused.cuh (kept in one place there; checked below)
 constexpr int kNBAR = 32;
@@ -40,6 +42,8 @@ static uint32_t max_rec(int q, int cols) {
         case MOE_Q4_K: return 9 * 512;
         case MOE_Q2_K: return 5 * 512 + 128;
         case MOE_Q8_0: return 17 * 512;
+        case MOE_Q6_K: return FQ6K::REC;
+        case MOE_Q3_K: return FQ3K::REC;
         default: {
             const int nb = cols / 32 < 8 ? cols / 32 : 8;
             return (uint32_t)nb * 512 + 256;
@@ -51,6 +55,8 @@ static size_t tile_bytes_of(int q, int cols) {
         case MOE_Q4_K: return FQ4K::tile_bytes(cols);
         case MOE_Q2_K: return FQ2K::tile_bytes(cols);
         case MOE_Q8_0: return FQ80::tile_bytes(cols);
+        case MOE_Q6_K: return FQ6K::tile_bytes(cols);
+        case MOE_Q3_K: return FQ3K::tile_bytes(cols);
         default: return FMX4::tile_bytes(cols);
     }
 }
@@ -162,6 +168,8 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
         case MOE_Q2_K: return launch_layer_q2k(a, sqtype, G, o.total, pdl, s);
         case MOE_Q8_0: return launch_layer_q80(a, sqtype, G, o.total, pdl, s);
         case MOE_MXFP4: return launch_layer_mx4(a, sqtype, G, o.total, pdl, s);
+        case MOE_Q6_K: return launch_layer_q6k(a, sqtype, G, o.total, pdl, s);
+        case MOE_Q3_K: return launch_layer_q3k(a, sqtype, G, o.total, pdl, s);
     }
     return cudaErrorNotSupported;
 }
@@ -172,7 +180,9 @@ using namespace moe;
 
 namespace {
 bool al16p(const void *p) { return ((uintptr_t)p & 15u) == 0; }
-bool fmt_ok(int q) { return q == MOE_Q8_0 || q == MOE_Q4_K || q == MOE_Q2_K || q == MOE_MXFP4; }
+bool fmt_ok(int q) {
+    return q == MOE_Q8_0 || q == MOE_Q4_K || q == MOE_Q2_K || q == MOE_MXFP4 || q == MOE_Q6_K || q == MOE_Q3_K;
+}
 bool cols_ok(int q, int cols) { return cols > 0 && (q == MOE_MXFP4 ? cols % 32 == 0 : cols % 256 == 0); }
 }  // namespace
 

@@ -257,6 +257,8 @@ __global__ void pack_kernel(const uint8_t *__restrict__ src, int qtype, int rows
         case MOE_Q4_K: nrec = FQ4K::nrec(cols); tile = FQ4K::tile_bytes(cols); row_bytes = (size_t)cols / 256 * 144; break;
         case MOE_Q2_K: nrec = FQ2K::nrec(cols); tile = FQ2K::tile_bytes(cols); row_bytes = (size_t)cols / 256 * 84; break;
         case MOE_Q8_0: nrec = FQ80::nrec(cols); tile = FQ80::tile_bytes(cols); row_bytes = (size_t)cols / 32 * 34; break;
+        case MOE_Q6_K: nrec = FQ6K::nrec(cols); tile = FQ6K::tile_bytes(cols); row_bytes = (size_t)cols / 256 * 210; break;
+        case MOE_Q3_K: nrec = FQ3K::nrec(cols); tile = FQ3K::tile_bytes(cols); row_bytes = (size_t)cols / 256 * 110; break;
         default: nrec = FMX4::nrec(cols); tile = FMX4::tile_bytes(cols); row_bytes = (size_t)cols / 32 * 17; break;
     }
     if (tid >= (long long)rows * nrec) return;
@@ -275,6 +277,17 @@ __global__ void pack_kernel(const uint8_t *__restrict__ src, int qtype, int rows
         for (int p = 0; p < 5; ++p)
             for (int i = 0; i < 16; ++i) o[p * 512 + lane * 16 + i] = b[16 * p + i];
         for (int i = 0; i < 4; ++i) o[5 * 512 + lane * 4 + i] = b[80 + i];
+    } else if (qtype == MOE_Q6_K) {
+        const uint8_t *b = s + (size_t)r * 210;
+        uint8_t *o = base + FQ6K::rec_off(cols, r);
+        for (int p = 0; p < 13; ++p)
+            for (int i = 0; i < 16; ++i) o[p * 512 + lane * 16 + i] = b[16 * p + i];
+        for (int i = 0; i < 4; ++i) o[13 * 512 + lane * 4 + i] = i < 2 ? b[208 + i] : 0;
+    } else if (qtype == MOE_Q3_K) {
+        const uint8_t *b = s + (size_t)r * 110;
+        uint8_t *o = base + FQ3K::rec_off(cols, r);
+        for (int p = 0; p < 7; ++p)
+            for (int i = 0; i < 16; ++i) o[p * 512 + lane * 16 + i] = (16 * p + i < 110) ? b[16 * p + i] : 0;
     } else if (qtype == MOE_Q8_0) {
         uint8_t *o = base + FQ80::rec_off(cols, r);
         for (int bb = 0; bb < 8; ++bb) {
@@ -330,6 +343,8 @@ __global__ void row_dots_kernel(const uint8_t *packed, int qtype, int cols, int 
     if (qtype == MOE_Q4_K) row_dots_fixed<FQ4K>(packed, cols, row, x, out);
     else if (qtype == MOE_Q2_K) row_dots_fixed<FQ2K>(packed, cols, row, x, out);
     else if (qtype == MOE_Q8_0) row_dots_fixed<FQ80>(packed, cols, row, x, out);
+    else if (qtype == MOE_Q6_K) row_dots_fixed<FQ6K>(packed, cols, row, x, out);
+    else if (qtype == MOE_Q3_K) row_dots_fixed<FQ3K>(packed, cols, row, x, out);
     else {
         const uint8_t *tile = packed + (size_t)(row >> 5) * FMX4::tile_bytes(cols);
         for (int r = 0; r < FMX4::nrec(cols); ++r) {

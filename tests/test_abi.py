@@ -59,8 +59,12 @@ def test_size_helpers():
     assert moe.moe_packed_bytes(moe.Q4_K, 33, 2048) == 0          # rows % 32
     assert moe.moe_packed_bytes(moe.Q4_K, 32, 2880) == 0          # K-quants need 256 columns
     assert moe.moe_packed_bytes(moe.F32, 32, 256) == 0
-    # codes 5 and 6 (Q6_K, Q3_K) exist on the oracle side only: the library refuses them
-    for code in (5, 6, 7, -1):
+    # Q6_K: a 4-byte {d, 0, 0} entry per row and block instead of the 2-byte d;
+    # Q3_K: 112 bytes per row and block instead of 110
+    assert moe.moe_packed_bytes(moe.Q6_K, 64, 2048) == 64 * 8 * 212
+    assert moe.moe_packed_bytes(moe.Q3_K, 64, 2048) == 64 * 8 * 112
+    assert moe.moe_packed_bytes(moe.Q6_K, 32, 2880) == 0 and moe.moe_packed_bytes(moe.Q3_K, 32, 2880) == 0
+    for code in (7, -1):
         assert moe.moe_packed_bytes(code, 32, 2048) == 0
 
 
@@ -90,11 +94,15 @@ def test_argument_errors_return_before_launch():
     assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, 1 << 20, None, 0, s) == INVALID
     pool = moe._Pool(moe.Q4_K, 2048, 544, 8, 1 << 20)                 # Q4_K needs 256-multiples
     assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, 1 << 20, None, 0, s) == UNSUP
-    for code in (5, 6):                                                # formats the kernels do not decode
+    for code in (7, -1):                                               # codes the library does not know
         assert L.moe_pack_weights(1 << 20, code, 32, 2048, 1 << 20, s) == UNSUP
         pool = moe._Pool(code, 2048, 512, 8, 1 << 20)
         assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, 1 << 20, None, 0,
                                 s) == INVALID
+    for code in (moe.Q6_K, moe.Q3_K):                                  # 256-column formats
+        pool = moe._Pool(code, 2048, 544, 8, 1 << 20)
+        assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, 1 << 20, None, 0,
+                                s) == UNSUP
     pool = moe._Pool(moe.Q4_K, 2048, 512, 8, 1 << 20)
     assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, 1 << 20, None, 0, s) == WS
     assert L.moe_expert_ffn(1 << 20, 0, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, 1 << 20, None, 0, s) == 0

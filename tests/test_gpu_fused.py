@@ -25,6 +25,13 @@ SMALL = {
     # holds 32 keys per lane; k = 32 is the largest selection
     "E1024 k32 T=1": (synth.shrink(synth.CONFIGS["a3b"], H=512, I=256, E=1024, k=32, shared_I=256), 1),
     "E1024 k32 T=3": (synth.shrink(synth.CONFIGS["a3b"], H=512, I=256, E=1024, k=32, shared_I=256), 3),
+    "q6_K + q6_K shared T=1": (synth.shrink(synth.CONFIGS["a3b"], H=1024, I=512, E=16, k=4, shared_I=256,
+                                            qtype=synth.Q6_K, shared_qtype=synth.Q6_K), 1),
+    "q6_K + q8_0 shared T=3": (synth.shrink(synth.CONFIGS["a3b"], H=1024, I=512, E=16, k=4, shared_I=256,
+                                            qtype=synth.Q6_K, shared_qtype=synth.Q8_0), 3),
+    "q3_K + q8_0 shared, q8_0 router T=1": (synth.shrink(synth.CONFIGS["wide"], H=1536, I=512, E=12, k=4,
+                                                         shared_I=512, qtype=synth.Q3_K), 1),
+    "q3_K T=4": (synth.shrink(synth.CONFIGS["a22b"], H=1024, I=768, E=24, k=4, qtype=synth.Q3_K), 4),
 }
 
 

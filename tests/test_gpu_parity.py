@@ -48,7 +48,8 @@ def test_quantize_bit_exact(n, T):
 # ----------------------------------------------------------- integer dots
 
 @pytest.mark.parametrize("qt,cols", [(synth.Q4_K, 2048), (synth.Q2_K, 1024), (synth.Q8_0, 512),
-                                     (synth.MXFP4, 2880), (synth.MXFP4, 256)])
+                                     (synth.MXFP4, 2880), (synth.MXFP4, 256), (synth.Q6_K, 2048),
+                                     (synth.Q3_K, 1536), (synth.Q6_K, 256), (synth.Q3_K, 7168)])
 def test_row_dots_bit_exact(qt, cols):
     rows = 64
     W = synth.matrix(qt, 3, 900 + qt, 0.02, rows, cols)
@@ -56,8 +57,8 @@ def test_row_dots_bit_exact(qt, cols):
     d, q, bs = oracle.quantize(x)
     rec = to_dev(pack_q8_records(d, q, bs))
     packed = moe.pack(to_dev(W), qt, rows, cols)
-    nsub = {synth.Q4_K: 8, synth.Q2_K: 16, synth.Q8_0: 1, synth.MXFP4: 1}[qt]
-    qk = {synth.Q4_K: 256, synth.Q2_K: 256, synth.Q8_0: 32, synth.MXFP4: 32}[qt]
+    nsub = {synth.Q4_K: 8, synth.Q2_K: 16, synth.Q8_0: 1, synth.MXFP4: 1, synth.Q6_K: 16, synth.Q3_K: 16}[qt]
+    qk = {synth.Q4_K: 256, synth.Q2_K: 256, synth.Q8_0: 32, synth.MXFP4: 32, synth.Q6_K: 256, synth.Q3_K: 256}[qt]
     n_out = cols // qk * nsub
     for row in (0, 1, 31, 32, 45, 63):
         out = torch.full((n_out + 8,), -7, dtype=torch.int32, device=DEV)
