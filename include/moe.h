@@ -160,6 +160,15 @@ moe_status moe_quantize_q8K(const float *x, int T, int n, void *xq, cudaStream_t
  *                 E (renormalize == 0).  Sigmoid: s = 1/(1+exp(-l)), divided
  *                 by the sum over the chosen k when renormalize != 0.
  *   logits_out  : device fp32 [T][E] out, or NULL
+ *   shared_gate : device fp32 [H], 16-byte aligned, or NULL: the shared
+ *                 expert's gate vector (the README's gate_inp_shexp, an f32
+ *                 tensor; its use is not stated there, and the reading taken
+ *                 is a per-token scalar gate on the shared expert's output)
+ *   shared_scale: device fp32 [T] out with shared_gate (NULL without it):
+ *                 sigma(shared_gate . hidden[t]), the logit in the fixed order
+ *                 below (a one-row F32 router, hidden required), then
+ *                 1/(1+exp(-l)); moe_expert_ffn takes it as the shared
+ *                 expert's weight
  *   ws          : device workspace of moe_route_workspace_bytes(T, E, H) bytes,
  *                 zero-filled before its first use; every completed call
  *                 leaves it ready for the next one
@@ -172,8 +181,9 @@ moe_status moe_quantize_q8K(const float *x, int T, int n, void *xq, cudaStream_t
  * segment, value (d_w*d_x)*isum.
  * Limits: 1 <= k <= min(E, MOE_MAX_K), E <= MOE_MAX_EXPERTS, T <= MOE_MAX_TOKENS,
  * H % 32 == 0.
- * Errors: MOE_ERR_INVALID_ARG for limits, gating, or a NULL or unaligned
- * buffer; MOE_ERR_UNSUPPORTED for a router type other than F32/Q8_0 or a Q8_0
+ * Errors: MOE_ERR_INVALID_ARG for limits, gating, a NULL or unaligned
+ * buffer, or shared_gate and shared_scale not given together (or a shared
+ * gate without hidden); MOE_ERR_UNSUPPORTED for a router type other than F32/Q8_0 or a Q8_0
  * router with H % 256 != 0; MOE_ERR_WORKSPACE for a missing, short or
  * unaligned ws.
  */
@@ -181,6 +191,7 @@ moe_status moe_route(const float *hidden, const void *xq, int T, int H,
                      const void *w_router, moe_qtype rtype, int E, const float *router_bias,
                      int k, moe_gating gating, int renormalize,
                      int32_t *ids, float *weights, float *logits_out,
+                     const float *shared_gate, float *shared_scale,
                      void *ws, size_t ws_bytes, cudaStream_t stream);
 size_t moe_route_workspace_bytes(int T, int E, int H);
 
@@ -213,12 +224,15 @@ typedef struct {
  *   xq      : device q8 records of the T hidden states (width pool->H),
  *             16-byte aligned
  *   ids     : device int32 [T][k]; weights: device fp32 [T][k]
- *   pool    : host pointer to the routed pool (qtype Q8_0, Q4_K, Q2_K or MXFP4)
- *   shared  : host pointer to a pool with E == 1 (weight 1, no biases read),
- *             or NULL
+ *   pool    : host pointer to the routed pool (qtype Q8_0, Q4_K, Q2_K, MXFP4,
+ *             Q6_K or Q3_K)
+ *   shared  : host pointer to a pool with E == 1 (no biases read), or NULL
+ *   shared_scale: device fp32 [T], the shared expert's weight per token
+ *             (moe_route's shared_scale), or NULL for weight 1; requires
+ *             shared
  *   y       : device fp32 [T][H] out, 16-byte aligned, overwritten:
  *             y[t] = sum over slots s in slot order of w[t][s]*o(ids[t][s])
- *                    + o_shared (added last),
+ *                    + g[t]*o_shared (added last; g = shared_scale or 1),
  *             o = W_down . q8(h) + b_down,  h = silu(g) * u,
  *             g = W_gate . xq + b_gate, u = W_up . xq + b_up (fp32 h is
  *             requantised with the moe_quantize_q8K rule, width I).
@@ -235,13 +249,14 @@ typedef struct {
  * Limits: T <= MOE_MAX_TOKENS, k <= MOE_MAX_K, E <= MOE_MAX_EXPERTS;
  * H and I multiples of 32 (of 256 for Q4_K, Q2_K, Q8_0).
  * Errors: MOE_ERR_INVALID_ARG for limits, a pool with no expert table, an
- * unknown expert format or a NULL or unaligned buffer; MOE_ERR_UNSUPPORTED
- * for widths the format cannot hold or a shared pool of another H;
+ * unknown expert format, a NULL or unaligned buffer, or shared_scale without
+ * a shared pool; MOE_ERR_UNSUPPORTED for widths the format cannot hold or a
+ * shared pool of another H;
  * MOE_ERR_WORKSPACE for a missing, short or unaligned ws.
  */
 moe_status moe_expert_ffn(const void *xq, int T, const int32_t *ids, const float *weights, int k,
-                          const moe_pool *pool, const moe_pool *shared, float *y,
-                          void *ws, size_t ws_bytes, cudaStream_t stream);
+                          const moe_pool *pool, const moe_pool *shared, const float *shared_scale,
+                          float *y, void *ws, size_t ws_bytes, cudaStream_t stream);
 size_t moe_ffn_workspace_bytes(int T, int k, const moe_pool *pool, const moe_pool *shared);
 
 /*
@@ -266,8 +281,8 @@ size_t moe_ffn_workspace_bytes(int T, int k, const moe_pool *pool, const moe_poo
  *    or repeated ids are still skipped.
  */
 moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, const float *weights, int k,
-                                  const moe_pool *pool, const moe_pool *shared, float *y,
-                                  cudaStream_t stream);
+                                  const moe_pool *pool, const moe_pool *shared, const float *shared_scale,
+                                  float *y, cudaStream_t stream);
 
 /*
  * The whole layer: quantise (moe_quantize_q8K's rule), route (moe_route's
@@ -286,6 +301,9 @@ moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, con
  * three calls (same arithmetic and summation orders).
  *   hidden      : device fp32 [T][H]; w_router/rtype/router_bias/k/gating/
  *                 renormalize as in moe_route; pool/shared as in moe_expert_ffn
+ *   shared_gate : device fp32 [H] or NULL, as in moe_route: the shared
+ *                 expert's output is scaled per token by sigma(gate . hidden)
+ *                 (requires shared; 16-byte aligned)
  *                 (shared: the same format as pool or Q8_0)
  *   y           : device fp32 [T][H] out
  *   ids_out, weights_out, logits_out, xq_out: optional outputs (NULL to skip)
@@ -312,7 +330,7 @@ moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, con
 #define MOE_LAYER_OVERLAP_PREVIOUS 0x1u
 moe_status moe_layer_forward(const float *hidden, int T, const void *w_router, moe_qtype rtype,
                              const float *router_bias, int k, moe_gating gating, int renormalize,
-                             const moe_pool *pool, const moe_pool *shared, float *y,
+                             const moe_pool *pool, const moe_pool *shared, const float *shared_gate, float *y,
                              int32_t *ids_out, float *weights_out, float *logits_out, void *xq_out,
                              void *ws, size_t ws_bytes, unsigned flags, cudaStream_t stream);
 size_t moe_layer_workspace_bytes(int T, int k, const moe_pool *pool, const moe_pool *shared);

@@ -72,7 +72,7 @@ def _lib():
             L.oracle_dequant_row.argtypes = [i, _P, i, _P]
             L.oracle_expert_ffn.restype = i
             L.oracle_expert_ffn.argtypes = [ctypes.POINTER(_Pool), ctypes.POINTER(_Pool), i, i,
-                                            _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+                                            _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
             _h = L
         return _h
 
@@ -187,11 +187,12 @@ def _pool(qtype, H, I, E, gate, up, down, bg=None, bu=None, bd=None, owned=None,
     return _Pool(qtype, H, I, E, *[_ptr(a) for a in arrs])
 
 
-def expert_ffn(layer, xq, ids, w, owned=None, shared=True, want_h=False):
+def expert_ffn(layer, xq, ids, w, owned=None, shared=True, want_h=False, shared_scale=None):
     """y [T, H] (fp64) for q8 activations xq=(d, q, bsum), ids [T, k], w [T, k].
 
     layer: a ``synth.Layer``.  owned: optional bool[E] ("not mine" slots are
-    skipped).  shared: include the shared expert (weight 1, added last)."""
+    skipped).  shared: include the shared expert, added last with weight
+    shared_scale[t] (fp64 [T]; 1 when None)."""
     cfg = layer.cfg
     T, k = ids.shape
     keep = []
@@ -204,6 +205,7 @@ def expert_ffn(layer, xq, ids, w, owned=None, shared=True, want_h=False):
     xd, xqq, xbs = (_c(a, t) for a, t in zip(xq, (np.float32, np.int8, np.int16)))
     ids = _c(ids, np.int32)
     w = _c(w, np.float64)
+    ss = None if shared_scale is None else _c(shared_scale, np.float64)
     y = np.zeros((T, cfg.H), np.float64)
     I = cfg.I
     BI = act_block(I)
@@ -213,7 +215,7 @@ def expert_ffn(layer, xq, ids, w, owned=None, shared=True, want_h=False):
     hbs = np.zeros((T, k, I // 16), np.int16) if want_h else None
     bad = _lib().oracle_expert_ffn(ctypes.byref(pool), ctypes.byref(sp) if sp is not None else None,
                                    T, k, xd.ctypes.data, xqq.ctypes.data, xbs.ctypes.data,
-                                   ids.ctypes.data, w.ctypes.data, y.ctypes.data,
+                                   ids.ctypes.data, w.ctypes.data, _ptr(ss), y.ctypes.data,
                                    _ptr(h), _ptr(hd), _ptr(hq), _ptr(hbs))
     if bad < 0:
         raise ValueError("expert_ffn: unsupported shape")
@@ -223,12 +225,25 @@ def expert_ffn(layer, xq, ids, w, owned=None, shared=True, want_h=False):
     return out
 
 
+def shared_gate(w_gate, x):
+    """Per-token shared-expert weight sigma(w . x) for the f32 gate vector
+    w_gate [H] (READING in oracle.c: the shared-expert gate tensor of the
+    pulsar README's qwen35moe notes).  The logit is a one-row router GEMV in
+    the router's fixed summation order (fp32, ``router_logits``); the sigmoid
+    is taken in fp64.  Returns (logit fp32 [T], weight fp64 [T])."""
+    l = router_logits(np.asarray(w_gate, np.float32).reshape(1, -1), x)[:, 0]
+    with np.errstate(over="ignore"):   # exp(-l) = inf for a very negative logit: weight 0
+        return l, 1.0 / (1.0 + np.exp(-l.astype(np.float64)))
+
+
 def layer_forward(layer, owned=None, shared=True, want_h=False):
     """The whole hot path for one synth.Layer: quantise, route, top-k, expert FFN."""
     cfg = layer.cfg
     xq = quantize(layer.x)
     logits = router_logits(layer.router, layer.x, cfg.router_qtype, layer.router_bias, xq=xq)
     ids, w = topk(logits, cfg.k, SIGMOID if cfg.gating == "sigmoid" else SOFTMAX, cfg.renorm)
-    res = expert_ffn(layer, xq, ids, w, owned=owned, shared=shared, want_h=want_h)
-    res.update(xq=xq, logits=logits, ids=ids, w=w)
+    sg = getattr(layer, "shexp_gate", None)
+    sg_l, sg_w = shared_gate(sg, layer.x) if (sg is not None and shared and cfg.has_shared) else (None, None)
+    res = expert_ffn(layer, xq, ids, w, owned=owned, shared=shared, want_h=want_h, shared_scale=sg_w)
+    res.update(xq=xq, logits=logits, ids=ids, w=w, shared_logit=sg_l, shared_scale=sg_w)
     return res

@@ -477,14 +477,21 @@ static void expert_o(const oracle_pool *p, int e, const float *hd, const int8_t 
 }
 
 /*
- * y[t][:] = sum_{s in slot order} w[t][s] * o(ids[t][s]) + o_shared (weight 1).
+ * y[t][:] = sum_{s in slot order} w[t][s] * o(ids[t][s]) + g[t] * o_shared,
+ * the shared expert added last with weight g[t] = shared_scale[t] (the
+ * sigmoid of its gate logit, READING below) or 1 when shared_scale is NULL.
+ * READING: the pulsar README names a shared-expert gate tensor
+ * (gate_inp_shexp, one of the f32 tensors it loads for qwen35moe) but does
+ * not state its use; the plain reading taken here is a per-token scalar
+ * sigma(w . x) with w the f32 vector and x the token's hidden state, that
+ * scales the shared expert's output.
  * xd/xq/xbs: the q8 activations of the T tokens (H wide).  Optional outputs
  * h_out [T][k][I] (fp32 h) and hq_* (the requantised h) for component checks.
  * Returns the number of skipped out-of-range ids (slots with e < 0 or e >= E).
  */
 int oracle_expert_ffn(const oracle_pool *pool, const oracle_pool *shared, int T, int k,
                       const float *xd, const int8_t *xq, const int16_t *xbs,
-                      const int32_t *ids, const double *w, double *y,
+                      const int32_t *ids, const double *w, const double *shared_scale, double *y,
                       float *h_out, float *hq_d, int8_t *hq_q, int16_t *hq_bs) {
     int H = pool->H, I = pool->I, BH = act_block(H), BI = act_block(I);
     int bad = 0;
@@ -517,7 +524,8 @@ int oracle_expert_ffn(const oracle_pool *pool, const oracle_pool *shared, int T,
             expert_h(shared, 0, xdt, xqt, xbt, h);
             oracle_quantize(h, Is, BS, hd, hq, hbs);
             expert_o(shared, 0, hd, hq, hbs, o);
-            for (int r = 0; r < H; ++r) yt[r] += o[r];
+            double g = shared_scale ? shared_scale[t] : 1.0;
+            for (int r = 0; r < H; ++r) yt[r] += g * o[r];
         }
     }
     return bad;

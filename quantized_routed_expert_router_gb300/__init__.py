@@ -69,16 +69,18 @@ def lib():
         L.moe_quantize_q8K.restype = i
         L.moe_quantize_q8K.argtypes = [_P, i, i, _P, _P]
         L.moe_route.restype = i
-        L.moe_route.argtypes = [_P, _P, i, i, _P, i, i, _P, i, i, i, _P, _P, _P, _P, sz, _P]
+        L.moe_route.argtypes = [_P, _P, i, i, _P, i, i, _P, i, i, i, _P, _P, _P, _P, _P, _P, sz, _P]
         L.moe_route_workspace_bytes.restype = sz
         L.moe_route_workspace_bytes.argtypes = [i, i, i]
         L.moe_expert_ffn.restype = i
-        L.moe_expert_ffn.argtypes = [_P, i, _P, _P, i, ctypes.POINTER(_Pool), ctypes.POINTER(_Pool), _P, _P, sz, _P]
+        L.moe_expert_ffn.argtypes = [_P, i, _P, _P, i, ctypes.POINTER(_Pool), ctypes.POINTER(_Pool), _P, _P, _P, sz,
+                                     _P]
         L.moe_expert_ffn_noalloc.restype = i
-        L.moe_expert_ffn_noalloc.argtypes = [_P, i, _P, _P, i, ctypes.POINTER(_Pool), ctypes.POINTER(_Pool), _P, _P]
+        L.moe_expert_ffn_noalloc.argtypes = [_P, i, _P, _P, i, ctypes.POINTER(_Pool), ctypes.POINTER(_Pool), _P, _P,
+                                             _P]
         L.moe_layer_forward.restype = i
         L.moe_layer_forward.argtypes = [_P, i, _P, i, _P, i, i, i, ctypes.POINTER(_Pool), ctypes.POINTER(_Pool),
-                                        _P, _P, _P, _P, _P, _P, sz, ctypes.c_uint, _P]
+                                        _P, _P, _P, _P, _P, _P, _P, sz, ctypes.c_uint, _P]
         L.moe_layer_workspace_bytes.restype = sz
         L.moe_layer_workspace_bytes.argtypes = [i, i, ctypes.POINTER(_Pool), ctypes.POINTER(_Pool)]
         L.moe_ffn_workspace_bytes.restype = sz
@@ -143,12 +145,14 @@ def moe_route_workspace_bytes(T: int, E: int, H: int) -> int:
 
 
 def moe_route(hidden, xq, w_router, rtype: int, E: int, router_bias, k: int, gating: int, renormalize: bool,
-              ids, weights, logits_out, ws, T: int | None = None, H: int | None = None, stream=None):
+              ids, weights, logits_out, ws, T: int | None = None, H: int | None = None, stream=None,
+              shared_gate=None, shared_scale=None):
     if T is None or H is None:
         T, H = hidden.shape
     _check(lib().moe_route(_ptr(hidden), _ptr(xq), T, H, _ptr(w_router), rtype, E, _ptr(router_bias), k, gating,
-                           int(bool(renormalize)), _ptr(ids), _ptr(weights), _ptr(logits_out), _ptr(ws),
-                           ws.numel() * ws.element_size(), _stream(stream)), "moe_route")
+                           int(bool(renormalize)), _ptr(ids), _ptr(weights), _ptr(logits_out), _ptr(shared_gate),
+                           _ptr(shared_scale), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_route")
 
 
 class ExpertPool:
@@ -193,18 +197,18 @@ def moe_ffn_workspace_bytes(T: int, k: int, pool: ExpertPool, shared: ExpertPool
 
 
 def moe_expert_ffn(xq, T: int, ids, weights, k: int, pool: ExpertPool, shared: ExpertPool | None, y, ws,
-                   stream=None):
+                   stream=None, shared_scale=None):
     _check(lib().moe_expert_ffn(_ptr(xq), T, _ptr(ids), _ptr(weights), k, ctypes.byref(pool.c),
-                                ctypes.byref(shared.c) if shared is not None else None, _ptr(y), _ptr(ws),
-                                ws.numel() * ws.element_size(), _stream(stream)), "moe_expert_ffn")
+                                ctypes.byref(shared.c) if shared is not None else None, _ptr(shared_scale), _ptr(y),
+                                _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "moe_expert_ffn")
 
 
 def moe_expert_ffn_noalloc(xq, T: int, ids, weights, k: int, pool: ExpertPool, shared: ExpertPool | None, y,
-                           stream=None):
+                           stream=None, shared_scale=None):
     """moe_expert_ffn with the library's fixed device scratch (no workspace, no allocation)."""
     _check(lib().moe_expert_ffn_noalloc(_ptr(xq), T, _ptr(ids), _ptr(weights), k, ctypes.byref(pool.c),
-                                        ctypes.byref(shared.c) if shared is not None else None, _ptr(y),
-                                        _stream(stream)), "moe_expert_ffn_noalloc")
+                                        ctypes.byref(shared.c) if shared is not None else None,
+                                        _ptr(shared_scale), _ptr(y), _stream(stream)), "moe_expert_ffn_noalloc")
 
 
 def moe_layer_workspace_bytes(T: int, k: int, pool: ExpertPool, shared: ExpertPool | None) -> int:
@@ -214,11 +218,13 @@ def moe_layer_workspace_bytes(T: int, k: int, pool: ExpertPool, shared: ExpertPo
 
 def moe_layer_forward(hidden, w_router, rtype: int, router_bias, k: int, gating: int, renormalize: bool,
                       pool: ExpertPool, shared: ExpertPool | None, y, ws, ids_out=None, weights_out=None,
-                      logits_out=None, xq_out=None, flags: int = 0, T: int | None = None, stream=None):
+                      logits_out=None, xq_out=None, flags: int = 0, T: int | None = None, stream=None,
+                      shared_gate=None):
     T = hidden.shape[0] if T is None else T
     _check(lib().moe_layer_forward(_ptr(hidden), T, _ptr(w_router), rtype, _ptr(router_bias), k, gating,
                                    int(bool(renormalize)), ctypes.byref(pool.c),
-                                   ctypes.byref(shared.c) if shared is not None else None, _ptr(y),
+                                   ctypes.byref(shared.c) if shared is not None else None, _ptr(shared_gate),
+                                   _ptr(y),
                                    _ptr(ids_out), _ptr(weights_out), _ptr(logits_out), _ptr(xq_out), _ptr(ws),
                                    ws.numel() * ws.element_size(), flags, _stream(stream)), "moe_layer_forward")
 

@@ -64,7 +64,7 @@ bool pool_shape_ok(const moe_pool *p) {
 
 namespace moe {
 moe_status ffn_check_args(const void *xq, int T, const int32_t *ids, const float *weights, int k,
-                          const moe_pool *pool, const moe_pool *shared, const float *y) {
+                          const moe_pool *pool, const moe_pool *shared, const float *shared_scale, const float *y) {
     if (T < 0 || T > MOE_MAX_TOKENS || k < 1 || k > MOE_MAX_K) return MOE_ERR_INVALID_ARG;
     if (!pool_ok(pool, false)) return MOE_ERR_INVALID_ARG;
     if (shared && !pool_ok(shared, true)) return MOE_ERR_INVALID_ARG;
@@ -72,6 +72,7 @@ moe_status ffn_check_args(const void *xq, int T, const int32_t *ids, const float
     if (shared && (shared->H != pool->H || !pool_shape_ok(shared))) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
     if (!xq || !ids || !weights || !y || !aligned16(xq) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    if (shared_scale && !shared) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 }  // namespace moe
@@ -108,7 +109,8 @@ size_t moe_route_workspace_bytes(int T, int E, int H) {
 
 moe_status moe_route(const float *hidden, const void *xq, int T, int H, const void *w_router, moe_qtype rtype,
                      int E, const float *router_bias, int k, moe_gating gating, int renormalize, int32_t *ids,
-                     float *weights, float *logits_out, void *ws, size_t ws_bytes, cudaStream_t stream) {
+                     float *weights, float *logits_out, const float *shared_gate, float *shared_scale, void *ws,
+                     size_t ws_bytes, cudaStream_t stream) {
     if (T < 0 || T > MOE_MAX_TOKENS || H <= 0 || H % 32 || E < 1 || E > MOE_MAX_EXPERTS) return MOE_ERR_INVALID_ARG;
     if (k < 1 || k > E || k > MOE_MAX_K) return MOE_ERR_INVALID_ARG;
     if (gating != MOE_GATE_SOFTMAX && gating != MOE_GATE_SIGMOID) return MOE_ERR_INVALID_ARG;
@@ -121,6 +123,8 @@ moe_status moe_route(const float *hidden, const void *xq, int T, int H, const vo
         if (H % 256) return MOE_ERR_UNSUPPORTED;
         if (!xq || !aligned16(xq)) return MOE_ERR_INVALID_ARG;
     }
+    if ((shared_gate == nullptr) != (shared_scale == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (shared_gate && (!hidden || !aligned16(hidden) || !aligned16(shared_gate))) return MOE_ERR_INVALID_ARG;
     if (!ws || ws_bytes < route_ws(T, E, H) || !aligned16(ws)) return MOE_ERR_WORKSPACE;
     RouteArgs a;
     a.hidden = hidden;
@@ -139,6 +143,12 @@ moe_status moe_route(const float *hidden, const void *xq, int T, int H, const vo
     a.nseg = (H + 1023) / 1024;
     a.gating = gating;
     a.renorm = renormalize ? 1 : 0;
+    a.shared_gate = shared_gate;
+    a.shared_scale = shared_scale;
+    if (shared_gate) {
+        const moe_status st = cuda_status(launch_shared_gate(hidden, T, H, shared_gate, shared_scale, stream));
+        if (st != MOE_OK) return st;
+    }
     return cuda_status(launch_route(a, rtype, stream));
 }
 
@@ -148,9 +158,9 @@ size_t moe_ffn_workspace_bytes(int T, int k, const moe_pool *pool, const moe_poo
 }
 
 moe_status moe_expert_ffn(const void *xq, int T, const int32_t *ids, const float *weights, int k,
-                          const moe_pool *pool, const moe_pool *shared, float *y, void *ws, size_t ws_bytes,
-                          cudaStream_t stream) {
-    const moe_status v = moe::ffn_check_args(xq, T, ids, weights, k, pool, shared, y);
+                          const moe_pool *pool, const moe_pool *shared, const float *shared_scale, float *y,
+                          void *ws, size_t ws_bytes, cudaStream_t stream) {
+    const moe_status v = moe::ffn_check_args(xq, T, ids, weights, k, pool, shared, shared_scale, y);
     if (v != MOE_OK || T == 0) return v;
     const FfnWs L = ffn_ws_layout(T, k, pool->H, pool->I, shared ? shared->I : 0);
     if (!ws || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
@@ -161,6 +171,7 @@ moe_status moe_expert_ffn(const void *xq, int T, const int32_t *ids, const float
     a.weights = weights;
     a.experts = pool->experts;
     a.shared = shared ? shared->experts : nullptr;
+    a.shared_scale = shared_scale;
     a.y = y;
     a.status = (unsigned *)(w + L.status);
     a.counters = (unsigned *)(w + L.counters);

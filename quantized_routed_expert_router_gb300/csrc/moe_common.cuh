@@ -532,6 +532,38 @@ struct FQ3K {
     }
 };
 
+// ---------------------------------------------------- shared-expert gate
+// Per-token weight of the shared expert, sigma(w . x), w the f32 gate vector
+// (the pulsar README names the tensor, gate_inp_shexp, among the f32 tensors
+// it loads for qwen35moe; its plain reading is this scalar gate).  One warp:
+// the logit in the router's fixed order - 1024-element segments, lane l
+// accumulating float4 chunks l, l + 32, ... with fmaf in element order, an
+// xor butterfly over 16, 8, 4, 2, 1, segments added in order - then
+// 1 / (1 + exp(-l)).  w and x 16-byte aligned; every lane returns the weight.
+__device__ __forceinline__ float shared_gate_weight(const float *w, const float *x, int H, int lane) {
+    float l = 0.f;
+    for (int s0 = 0; s0 < H; s0 += 1024) {
+        const int seglen = min(1024, H - s0);
+        float v = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int c = lane + 32 * j;
+            if (4 * c < seglen) {
+                const float4 wv = *reinterpret_cast<const float4 *>(w + s0 + 4 * c);
+                const float4 xv = *reinterpret_cast<const float4 *>(x + s0 + 4 * c);
+                v = __fmaf_rn(wv.x, xv.x, v);
+                v = __fmaf_rn(wv.y, xv.y, v);
+                v = __fmaf_rn(wv.z, xv.z, v);
+                v = __fmaf_rn(wv.w, xv.w, v);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+        l = s0 == 0 ? v : __fadd_rn(l, v);
+    }
+    return 1.f / (1.f + expf(-l));
+}
+
 // ------------------------------------------------------------ quantiser
 // Activation quantisation rule (pulsar README, "MoE resolve": activations
 // quantised to q8_0/q8_K before integer dots).  Per block of B = 256 (32 where

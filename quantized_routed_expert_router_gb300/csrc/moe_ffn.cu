@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(FT) down_kernel(FfnArgs a) {
         if (a.shared) {
             float o = 0.f;
             for (int r = 0; r < ns; ++r) o += part[((size_t)(P + t) * nrec_max + r) * 32 + l];
-            y += o;
+            y += a.shared_scale ? a.shared_scale[t] * o : o;
         }
         a.y[(size_t)t * a.H + row] = y;
     }

@@ -177,6 +177,7 @@ struct Misc {
     int bt_j[64], bt_it[65], bt_rec[65], bt_slot[64];
     uint32_t bsum[MAX_LW], target, lo, hi;   // B shares, in 128-byte lines
     int closed;          // the B shares need no clamping (closed form)
+    float sgate[4];      // per-token weight of the shared expert (with a gate vector)
     int brev;            // B ranges are given to blocks G-1 first
 };
 
@@ -923,7 +924,8 @@ struct LayerKernel {
             }
             if (a.shared) {
                 const tword *ps = a.o_s + (size_t)t * a.H + row;
-                y += tag_value(wait_tag(ps, ld_tag(ps)));
+                const float os = tag_value(wait_tag(ps, ld_tag(ps)));
+                y += a.shared_gate ? m->sgate[t] * os : os;
             }
             a.y[(size_t)t * a.H + row] = y;
         }
@@ -1147,6 +1149,11 @@ struct LayerKernel {
         // (one call site per step: every inlined copy is code each launch fetches)
         const bool split = NT == 1 && !x_done;
         if (!x_done && (!split || warp > 0)) quantise_x(split ? 1 : 0);
+        if (a.shared_gate && warp == LW - 1)
+            for (int t = 0; t < a.T; ++t) {
+                const float s = shared_gate_weight(a.shared_gate, a.x + (size_t)t * a.H, a.H, lane);
+                if (lane == 0) m->sgate[t] = s;
+            }
         if (!split || warp == 0) poll_logits(split ? lane : threadIdx.x, split ? 32 : LW * 32);
         if (split) __syncwarp();
         else cbar();

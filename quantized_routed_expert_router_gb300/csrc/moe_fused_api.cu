@@ -196,7 +196,7 @@ constexpr int kFusedMaxTokens = 4;
 // workspace first (its status word is the layer's), then the router's, the
 // q8 activations, ids and weights
 struct SplitWs {
-    size_t ffn, route, xq, ids, w, total;
+    size_t ffn, route, xq, ids, w, sscale, total;
 };
 SplitWs split_ws_layout(int T, int k, const moe_pool *pool, const moe_pool *shared) {
     auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
@@ -206,7 +206,8 @@ SplitWs split_ws_layout(int T, int k, const moe_pool *pool, const moe_pool *shar
     s.xq = al(s.route + moe_route_workspace_bytes(T, pool->E, pool->H));
     s.ids = al(s.xq + (size_t)T * q8_row_bytes(pool->H));
     s.w = al(s.ids + 4 * (size_t)T * k);
-    s.total = al(s.w + 4 * (size_t)T * k);
+    s.sscale = al(s.w + 4 * (size_t)T * k);
+    s.total = al(s.sscale + 4 * (size_t)T);
     return s;
 }
 
@@ -220,7 +221,8 @@ size_t moe_layer_workspace_bytes(int T, int k, const moe_pool *pool, const moe_p
 
 moe_status moe_layer_forward(const float *hidden, int T, const void *w_router, moe_qtype rtype,
                              const float *router_bias, int k, moe_gating gating, int renormalize,
-                             const moe_pool *pool, const moe_pool *shared, float *y, int32_t *ids_out,
+                             const moe_pool *pool, const moe_pool *shared, const float *shared_gate, float *y,
+                             int32_t *ids_out,
                              float *weights_out, float *logits_out, void *xq_out, void *ws, size_t ws_bytes,
                              unsigned flags, cudaStream_t stream) {
     if (T < 0 || T > MOE_MAX_TOKENS || k < 1 || k > MOE_MAX_K) return MOE_ERR_INVALID_ARG;
@@ -236,6 +238,7 @@ moe_status moe_layer_forward(const float *hidden, int T, const void *w_router, m
     if (!cols_ok(pool->qtype, H) || !cols_ok(pool->qtype, I)) return MOE_ERR_UNSUPPORTED;
     if (shared && (!cols_ok(shared->qtype, H) || !cols_ok(shared->qtype, shared->I))) return MOE_ERR_UNSUPPORTED;
     if (shared && shared->qtype != pool->qtype && shared->qtype != MOE_Q8_0) return MOE_ERR_UNSUPPORTED;
+    if (shared_gate && (!shared || !al16p(shared_gate))) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
     if (!hidden || !w_router || !y || !al16p(hidden) || !al16p(w_router) || !al16p(y)) return MOE_ERR_INVALID_ARG;
     if (xq_out && !al16p(xq_out)) return MOE_ERR_INVALID_ARG;
@@ -246,11 +249,13 @@ moe_status moe_layer_forward(const float *hidden, int T, const void *w_router, m
         void *xq = xq_out ? xq_out : (void *)(w + S.xq);
         int32_t *ids = ids_out ? ids_out : (int32_t *)(w + S.ids);
         float *wts = weights_out ? weights_out : (float *)(w + S.w);
+        float *sscale = shared_gate ? (float *)(w + S.sscale) : nullptr;
         moe_status st = moe_quantize_q8K(hidden, T, H, xq, stream);
         if (st == MOE_OK)
             st = moe_route(hidden, xq, T, H, w_router, rtype, E, router_bias, k, gating, renormalize, ids, wts,
-                           logits_out, w + S.route, S.xq - S.route, stream);
-        if (st == MOE_OK) st = moe_expert_ffn(xq, T, ids, wts, k, pool, shared, y, w + S.ffn, S.route, stream);
+                           logits_out, shared_gate, sscale, w + S.route, S.xq - S.route, stream);
+        if (st == MOE_OK)
+            st = moe_expert_ffn(xq, T, ids, wts, k, pool, shared, sscale, y, w + S.ffn, S.route, stream);
         return st;
     }
     const LayerWs L = layer_ws_layout(T, k, H, I, shared ? shared->I : 0, E);
@@ -262,6 +267,7 @@ moe_status moe_layer_forward(const float *hidden, int T, const void *w_router, m
     a.rbias = router_bias;
     a.experts = pool->experts;
     a.shared = shared ? shared->experts : nullptr;
+    a.shared_gate = shared_gate;
     a.y = y;
     a.ids_out = ids_out;
     a.w_out = weights_out;

@@ -245,6 +245,20 @@ cudaError_t launch_route(const RouteArgs &a, int rtype, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------ shared-expert gate
+__global__ void __launch_bounds__(32) shared_gate_kernel(const float *__restrict__ hidden, int H,
+                                                         const float *__restrict__ w, float *__restrict__ scale) {
+    const int t = blockIdx.x;
+    const float s = shared_gate_weight(w, hidden + (size_t)t * H, H, threadIdx.x);
+    if (threadIdx.x == 0) scale[t] = s;
+}
+
+cudaError_t launch_shared_gate(const float *hidden, int T, int H, const float *w, float *scale, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    shared_gate_kernel<<<T, 32, 0, s>>>(hidden, H, w, scale);
+    return cudaGetLastError();
+}
+
 // ----------------------------------------------------------------- packing
 // One thread per (row, record): copies that row's bytes of the record from
 // the GGUF block row into the record's planes (layout stated in moe.h).

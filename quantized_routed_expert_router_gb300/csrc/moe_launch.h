@@ -23,6 +23,8 @@ struct RouteArgs {
     float *logits_out;
     float *partial;      // ws: [T][E][nseg]
     unsigned *counter;   // ws
+    const float *shared_gate;   // [H] or nullptr
+    float *shared_scale;        // [T] out (with shared_gate)
     int T, H, E, k, nseg, gating, renorm;
 };
 
@@ -32,6 +34,7 @@ struct FfnArgs {
     const float *weights;        // [T][k]
     const moe_expert *experts;   // device [E]
     const moe_expert *shared;    // device [1] or nullptr
+    const float *shared_scale;   // [T] weight of the shared expert, or nullptr (1)
     float *y;                    // [T][H]
     unsigned *status;            // ws
     unsigned *counters;          // ws [MAXP + 1]
@@ -54,6 +57,7 @@ struct LayerArgs {
     const float *rbias;
     const moe_expert *experts;      // device [E]
     const moe_expert *shared;       // device [1] or nullptr
+    const float *shared_gate;       // [H] gate vector of the shared expert, or nullptr
     float *y;                       // [T][H]
     int32_t *ids_out;               // optional outputs
     float *w_out;
@@ -84,7 +88,7 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
 // every argument check of moe_expert_ffn except the workspace's (MOE_OK for
 // T == 0 once the shapes are valid)
 moe_status ffn_check_args(const void *xq, int T, const int32_t *ids, const float *weights, int k,
-                          const moe_pool *pool, const moe_pool *shared, const float *y);
+                          const moe_pool *pool, const moe_pool *shared, const float *shared_scale, const float *y);
 
 // workspace layout of moe_expert_ffn (offsets in bytes)
 struct FfnWs {
@@ -97,6 +101,8 @@ int smem_optin();
 
 cudaError_t launch_quantize(const float *x, int T, int n, uint8_t *xq, cudaStream_t s);
 cudaError_t launch_route(const RouteArgs &a, int rtype, cudaStream_t s);
+// per-token weight of the shared expert (shared_gate_weight) into scale[T]
+cudaError_t launch_shared_gate(const float *hidden, int T, int H, const float *w, float *scale, cudaStream_t s);
 cudaError_t launch_pack(const uint8_t *src, int qtype, int rows, int cols, uint8_t *dst, cudaStream_t s);
 cudaError_t launch_row_dots(const uint8_t *packed, int qtype, int cols, int row, const uint8_t *xq,
                             int32_t *out, cudaStream_t s);

@@ -49,11 +49,11 @@ cudaError_t scratch_for_current_device(void **out) {
 using namespace moe;
 
 extern "C" moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, const float *weights,
-                                             int k, const moe_pool *pool, const moe_pool *shared, float *y,
-                                             cudaStream_t stream) {
+                                             int k, const moe_pool *pool, const moe_pool *shared,
+                                             const float *shared_scale, float *y, cudaStream_t stream) {
     // every check moe_expert_ffn makes comes first, so a call it would reject
     // enqueues nothing (not even the clear of the shared scratch below)
-    const moe_status v = ffn_check_args(xq, T, ids, weights, k, pool, shared, y);
+    const moe_status v = ffn_check_args(xq, T, ids, weights, k, pool, shared, shared_scale, y);
     if (v != MOE_OK) return v;
     const FfnWs L = ffn_ws_layout(T, k, pool->H, pool->I, shared ? shared->I : 0);
     if (L.total > kStaticScratchBytes) return MOE_ERR_WORKSPACE;   // beyond the fixed scratch
@@ -63,5 +63,6 @@ extern "C" moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_
     // the array keeps the previous call's contents: the status word and the
     // tickets must start at zero
     if (cudaMemsetAsync(scratch, 0, L.h_r, stream) != cudaSuccess) return MOE_ERR_CUDA;
-    return moe_expert_ffn(xq, T, ids, weights, k, pool, shared, y, scratch, kStaticScratchBytes, stream);
+    return moe_expert_ffn(xq, T, ids, weights, k, pool, shared, shared_scale, y, scratch, kStaticScratchBytes,
+                          stream);
 }

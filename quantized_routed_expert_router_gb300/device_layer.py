@@ -60,6 +60,8 @@ class DeviceLayer:
             self.sup, _ = pack_stack(L.sup, qs, Is, H, device)
             self.sdown, _ = pack_stack(L.sdown, qs, H, Is, device)
             self.shared = ExpertPool(qs, H, Is, [dict(gate=self.sgate, up=self.sup, down=self.sdown)], self.device)
+        shg = getattr(L, "shexp_gate", None)   # the shared expert's gate vector, if the layer has one
+        self.shared_gate = None if (shg is None or self.shared is None) else _dev(shg, device)
         self.alloc(self.T)
 
     def make_pool(self, owned=None) -> ExpertPool:
@@ -83,6 +85,7 @@ class DeviceLayer:
         self.w = torch.empty((T, self.k), dtype=torch.float32, device=d)
         self.logits = torch.empty((T, self.E), dtype=torch.float32, device=d)
         self.y = torch.empty((T, self.H), dtype=torch.float32, device=d)
+        self.shared_scale = torch.empty(T, dtype=torch.float32, device=d) if self.shared_gate is not None else None
         self.ws_route = torch.zeros(moe_route_workspace_bytes(T, self.E, self.H), dtype=torch.uint8, device=d)
         self.ws_ffn = torch.zeros(moe_ffn_workspace_bytes(T, self.k, self.pool, self.shared), dtype=torch.uint8,
                                   device=d)
@@ -95,13 +98,15 @@ class DeviceLayer:
     def route(self, x=None, stream=None, logits=True):
         x = self.x if x is None else x
         moe_route(x, self.xq, self.router, self.router_qtype, self.E, self.router_bias, self.k, self.gating,
-                  self.renorm, self.ids, self.w, self.logits if logits else None, self.ws_route, stream=stream)
+                  self.renorm, self.ids, self.w, self.logits if logits else None, self.ws_route, stream=stream,
+                  shared_gate=self.shared_gate, shared_scale=self.shared_scale)
 
     def ffn(self, ids=None, w=None, pool=None, shared="default", y=None, stream=None, T=None):
         T = self.T if T is None else T
+        sh = self.shared if shared == "default" else shared
         moe_expert_ffn(self.xq, T, self.ids if ids is None else ids, self.w if w is None else w, self.k,
-                       self.pool if pool is None else pool, self.shared if shared == "default" else shared,
-                       self.y if y is None else y, self.ws_ffn, stream)
+                       self.pool if pool is None else pool, sh, self.y if y is None else y, self.ws_ffn, stream,
+                       shared_scale=self.shared_scale if sh is not None else None)
 
     def forward(self, x=None, stream=None, logits=True):
         """three calls: moe_quantize_q8K, moe_route, moe_expert_ffn"""
@@ -113,10 +118,11 @@ class DeviceLayer:
     def forward_fused(self, x=None, stream=None, outputs=True, flags=0, pool=None, shared="default", y=None):
         """one call: moe_layer_forward"""
         x = self.x if x is None else x
+        sh = self.shared if shared == "default" else shared
         moe_layer_forward(x, self.router, self.router_qtype, self.router_bias, self.k, self.gating, self.renorm,
-                          self.pool if pool is None else pool, self.shared if shared == "default" else shared,
+                          self.pool if pool is None else pool, sh,
                           self.y if y is None else y, self.ws_layer,
                           ids_out=self.ids if outputs else None, weights_out=self.w if outputs else None,
                           logits_out=self.logits if outputs else None, xq_out=self.xq if outputs else None,
-                          flags=flags, stream=stream)
+                          flags=flags, stream=stream, shared_gate=self.shared_gate if sh is not None else None)
         return self.y

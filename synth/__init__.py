@@ -27,8 +27,7 @@ _SO = os.path.join(_HERE, "_synth.so")
 _lock = threading.Lock()
 _lib_handle = None
 
-# qtype codes: 0..4 are the library's public enum; Q6_K and Q3_K are generated
-# for the CPU oracle only (the library rejects those codes)
+# qtype codes: the library's public enum (moe_qtype)
 F32, Q8_0, Q4_K, Q2_K, MXFP4, Q6_K, Q3_K = 0, 1, 2, 3, 4, 5, 6
 QTYPE_NAMES = {F32: "f32", Q8_0: "q8_0", Q4_K: "q4_K", Q2_K: "q2_K", MXFP4: "mxfp4", Q6_K: "q6_K",
                Q3_K: "q3_K"}
@@ -123,6 +122,7 @@ class MoEConfig:
     router_qtype: int = F32
     shared_I: int = 0          # 0: no shared expert
     shared_qtype: int = -1
+    shared_gate: bool = False  # a sigmoid gate vector on the shared expert (f32 [H])
     biases: bool = False
     layers: int = 1
     tokens: tuple = (1,)
@@ -154,7 +154,7 @@ CONFIGS = {
 
 # tensor codes inside a stream id
 _T_X, _T_ROUTER, _T_GATE, _T_UP, _T_DOWN, _T_BG, _T_BU, _T_BD = 1, 2, 3, 4, 5, 6, 7, 8
-_T_SGATE, _T_SUP, _T_SDOWN = 9, 10, 11
+_T_SGATE, _T_SUP, _T_SDOWN, _T_SHGATE = 9, 10, 11, 12
 SIG_W, SIG_B, SIG_X, SIG_R = 0.02, 0.01, 1.0, 0.02
 
 
@@ -188,6 +188,7 @@ class Layer:
     sgate: np.ndarray | None = None    # uint8 [1, Is, row_bytes(H)]
     sup: np.ndarray | None = None
     sdown: np.ndarray | None = None
+    shexp_gate: np.ndarray | None = None   # float32 [H]: the shared expert's gate vector
     extra: dict = field(default_factory=dict)
 
 
@@ -230,6 +231,8 @@ def make_layer(cfg: MoEConfig, layer: int = 0, T: int = 1, seed: int = 0,
         L.sgate = matrix(qs, seed, stream_id(c, _T_SGATE, layer), SIG_W, Is, H)[None]
         L.sup = matrix(qs, seed, stream_id(c, _T_SUP, layer), SIG_W, Is, H)[None]
         L.sdown = matrix(qs, seed, stream_id(c, _T_SDOWN, layer), SIG_W, H, Is)[None]
+        if cfg.shared_gate:
+            L.shexp_gate = normal(seed, stream_id(c, _T_SHGATE, layer), SIG_R, 1, H)[0]
     return L
 
 

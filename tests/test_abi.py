@@ -78,7 +78,7 @@ def test_argument_errors_return_before_launch():
     assert L.moe_quantize_q8K(None, 1, 100, None, s) == UNSUP
     assert L.moe_quantize_q8K(None, 1, 256, None, s) == INVALID
     assert L.moe_quantize_q8K(None, 0, 256, None, s) == 0          # T = 0: no-op
-    args = [None, None, 1, 512, None, moe.F32, 16, None, 2, 0, 1, None, None, None, None, 0, s]
+    args = [None, None, 1, 512, None, moe.F32, 16, None, 2, 0, 1, None, None, None, None, None, None, 0, s]
     assert L.moe_route(*args) == INVALID                            # NULL router
     bad_k = list(args); bad_k[8] = 17
     assert L.moe_route(*bad_k) == INVALID                            # k > E
@@ -89,23 +89,23 @@ def test_argument_errors_return_before_launch():
     ok_ptrs = list(args)
     ok_ptrs[0] = ok_ptrs[4] = ok_ptrs[11] = ok_ptrs[12] = 1 << 20
     assert L.moe_route(*ok_ptrs) == WS                               # missing workspace
-    assert L.moe_expert_ffn(None, 1, None, None, 2, None, None, None, None, 0, s) == INVALID
+    assert L.moe_expert_ffn(None, 1, None, None, 2, None, None, None, None, None, 0, s) == INVALID
     pool = moe._Pool(moe.Q4_K, 2048, 500, 8, 1 << 20)                 # I not a multiple of 32
-    assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, 1 << 20, None, 0, s) == INVALID
+    assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, None, 1 << 20, None, 0, s) == INVALID
     pool = moe._Pool(moe.Q4_K, 2048, 544, 8, 1 << 20)                 # Q4_K needs 256-multiples
-    assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, 1 << 20, None, 0, s) == UNSUP
+    assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, None, 1 << 20, None, 0, s) == UNSUP
     for code in (7, -1):                                               # codes the library does not know
         assert L.moe_pack_weights(1 << 20, code, 32, 2048, 1 << 20, s) == UNSUP
         pool = moe._Pool(code, 2048, 512, 8, 1 << 20)
-        assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, 1 << 20, None, 0,
+        assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, None, 1 << 20, None, 0,
                                 s) == INVALID
     for code in (moe.Q6_K, moe.Q3_K):                                  # 256-column formats
         pool = moe._Pool(code, 2048, 544, 8, 1 << 20)
-        assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, 1 << 20, None, 0,
+        assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, None, 1 << 20, None, 0,
                                 s) == UNSUP
     pool = moe._Pool(moe.Q4_K, 2048, 512, 8, 1 << 20)
-    assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, 1 << 20, None, 0, s) == WS
-    assert L.moe_expert_ffn(1 << 20, 0, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, 1 << 20, None, 0, s) == 0
+    assert L.moe_expert_ffn(1 << 20, 1, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, None, 1 << 20, None, 0, s) == WS
+    assert L.moe_expert_ffn(1 << 20, 0, 1 << 20, 1 << 20, 2, ctypes.byref(pool), None, None, 1 << 20, None, 0, s) == 0
     assert L.moe_debug_row_dots(None, moe.Q4_K, 32, 256, 0, None, None, s) == INVALID
     assert moe.status_str(3).startswith("workspace")
 
@@ -128,7 +128,7 @@ def test_layer_call_sizes_and_argument_errors():
 
     def call(T=1, k=8, pool_=pool, shared_=shared, rtype=moe.F32, ws=None, ws_bytes=0, hidden=P):
         return L.moe_layer_forward(hidden, T, P, rtype, None, k, 0, 1, ctypes.byref(pool_),
-                                   ctypes.byref(shared_) if shared_ is not None else None, P,
+                                   ctypes.byref(shared_) if shared_ is not None else None, None, P,
                                    None, None, None, None, ws, ws_bytes, 0, s)
 
     assert call(T=17) == INVALID                  # above the token limit
@@ -160,14 +160,14 @@ def test_documented_alignment_errors():
     P = 1 << 20
     assert L.moe_quantize_q8K(P + 4, 1, 256, P, s) == INVALID          # x
     assert L.moe_quantize_q8K(P, 1, 256, P + 8, s) == INVALID          # xq
-    args = [P, None, 1, 512, P, moe.F32, 16, None, 2, 0, 1, P, P, None, P, 1 << 16, s]
+    args = [P, None, 1, 512, P, moe.F32, 16, None, 2, 0, 1, P, P, None, None, None, P, 1 << 16, s]
     bad_h = list(args); bad_h[0] = P + 4
     assert L.moe_route(*bad_h) == INVALID                               # hidden, F32 router
     bad_w = list(args); bad_w[4] = P + 4
     assert L.moe_route(*bad_w) == INVALID                               # router rows
     pool = moe._Pool(moe.Q4_K, 2048, 512, 8, P)
-    ffn = [P, 1, P, P, 2, ctypes.byref(pool), None, P, None, 0, s]
-    bad_y = list(ffn); bad_y[7] = P + 4
+    ffn = [P, 1, P, P, 2, ctypes.byref(pool), None, None, P, None, 0, s]
+    bad_y = list(ffn); bad_y[8] = P + 4
     assert L.moe_expert_ffn(*bad_y) == INVALID                          # y
     bad_x = list(ffn); bad_x[0] = P + 8
     assert L.moe_expert_ffn(*bad_x) == INVALID                          # xq

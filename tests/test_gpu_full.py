@@ -15,14 +15,17 @@ moe = pytest.importorskip("quantized_routed_expert_router_gb300")
 from quantized_routed_expert_router_gb300.device_layer import DeviceLayer  # noqa: E402
 
 CASES = [("tiny", 1), ("a3b", 1), ("oss20b", 1), ("oss20b", 4), ("wide", 1), ("a22b", 1), ("a22b", 4),
-         ("a22b", 16), ("a3b/q6_K", 1), ("a3b/q6_K", 4), ("wide/q3_K", 1), ("wide/q3_K", 4), ("a3b/q3_K", 16)]
+         ("a22b", 16), ("a3b/q6_K", 1), ("a3b/q6_K", 4), ("wide/q3_K", 1), ("wide/q3_K", 4), ("a3b/q3_K", 16),
+         ("a3b/gated", 1), ("a3b/gated", 16)]
 
 # the two further routed-expert formats on full-size shapes: the 35B-A3B-style
 # layer with Q6_K routed and shared experts, and the wide layer with Q3_K
 # routed experts (Q8_0 shared expert and router as in that workload)
 VARIANTS = {"a3b/q6_K": ("a3b", dict(qtype=synth.Q6_K, shared_qtype=synth.Q6_K)),
             "wide/q3_K": ("wide", dict(qtype=synth.Q3_K)),
-            "a3b/q3_K": ("a3b", dict(qtype=synth.Q3_K, shared_qtype=synth.Q8_0))}
+            "a3b/q3_K": ("a3b", dict(qtype=synth.Q3_K, shared_qtype=synth.Q8_0)),
+            # the 35B-A3B-style layer with a sigmoid gate on its shared expert
+            "a3b/gated": ("a3b", dict(shared_gate=True))}
 
 
 def config(name):

@@ -32,6 +32,13 @@ SMALL = {
     "q3_K + q8_0 shared, q8_0 router T=1": (synth.shrink(synth.CONFIGS["wide"], H=1536, I=512, E=12, k=4,
                                                          shared_I=512, qtype=synth.Q3_K), 1),
     "q3_K T=4": (synth.shrink(synth.CONFIGS["a22b"], H=1024, I=768, E=24, k=4, qtype=synth.Q3_K), 4),
+    # the shared expert scaled per token by sigma(gate . x)
+    "q4_K + gated shared T=1": (synth.shrink(synth.CONFIGS["a3b"], H=1024, I=512, E=16, k=4, shared_I=256,
+                                             shared_gate=True), 1),
+    "q4_K + gated shared T=3": (synth.shrink(synth.CONFIGS["a3b"], H=1024, I=512, E=16, k=4, shared_I=256,
+                                             shared_gate=True), 3),
+    "q2_K + gated q8_0 shared, q8_0 router T=2": (synth.shrink(synth.CONFIGS["wide"], H=1536, I=512, E=12, k=4,
+                                                               shared_I=512, shared_gate=True), 2),
 }
 
 

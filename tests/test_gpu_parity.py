@@ -260,3 +260,24 @@ def test_zero_tokens_and_errors():
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_expert_ffn(dl.xq, 17, dl.ids, dl.w, dl.k, dl.pool, None, dl.y, dl.ws_ffn)
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("T", [1, 5, 16])
+@pytest.mark.parametrize("H", [512, 2880, 7168])
+def test_route_shared_gate_weight(T, H):
+    """moe_route's per-token shared-expert weight sigma(w . x): the fp32 logit
+    in the router's fixed order (bit-exact with the oracle's one-row router)
+    through fp32 exp, against the oracle's fp64 sigmoid of the same logit."""
+    E, k = 16, 2
+    W = synth.normal(7, H, 0.02, E, H)
+    g = synth.normal(7, H + 1, 0.02, 1, H)[0]
+    x = synth.normal(7, H + 2, 1.0, T, H)
+    _, want = oracle.shared_gate(g, x)
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    sc = torch.full((T,), float("nan"), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(moe.moe_route_workspace_bytes(T, E, H), dtype=torch.uint8, device=DEV)
+    moe.moe_route(to_dev(x), None, to_dev(W), synth.F32, E, None, k, oracle.SOFTMAX, True, ids, w, None, ws,
+                  shared_gate=to_dev(g), shared_scale=sc)
+    torch.cuda.synchronize()
+    assert np.allclose(sc.cpu().numpy(), want, rtol=1e-6, atol=0)

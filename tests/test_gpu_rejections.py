@@ -30,12 +30,12 @@ def test_rejected_calls_touch_nothing():
     pool, shared = ctypes.byref(dl.pool.c), ctypes.byref(dl.shared.c)
     ffn_ws = L.moe_ffn_workspace_bytes(2, cfg.k, pool, shared)
     # FFN: workspace one byte short, unaligned y, out-of-range k
-    assert L.moe_expert_ffn(_p(dl.xq), 2, _p(dl.ids), _p(dl.w), cfg.k, pool, shared, _p(y), _p(dl.ws_ffn),
+    assert L.moe_expert_ffn(_p(dl.xq), 2, _p(dl.ids), _p(dl.w), cfg.k, pool, shared, None, _p(y), _p(dl.ws_ffn),
                             ffn_ws - 1, s) == WS
     y_off = ctypes.c_void_p(y.data_ptr() + 4)
-    assert L.moe_expert_ffn(_p(dl.xq), 2, _p(dl.ids), _p(dl.w), cfg.k, pool, shared, y_off, _p(dl.ws_ffn),
+    assert L.moe_expert_ffn(_p(dl.xq), 2, _p(dl.ids), _p(dl.w), cfg.k, pool, shared, None, y_off, _p(dl.ws_ffn),
                             ffn_ws, s) == INVALID
-    assert L.moe_expert_ffn(_p(dl.xq), 2, _p(dl.ids), _p(dl.w), 0, pool, shared, _p(y), _p(dl.ws_ffn),
+    assert L.moe_expert_ffn(_p(dl.xq), 2, _p(dl.ids), _p(dl.w), 0, pool, shared, None, _p(y), _p(dl.ws_ffn),
                             ffn_ws, s) == INVALID
     # layer call: workspace one byte short (both dispatch paths)
     for T in (2, 8):
@@ -43,14 +43,14 @@ def test_rejected_calls_touch_nothing():
         ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
         x = torch.zeros((T, cfg.H), dtype=torch.float32, device="cuda")
         yT = torch.full((T, cfg.H), float("nan"), device="cuda")
-        assert L.moe_layer_forward(_p(x), T, _p(dl.router), moe.F32, None, cfg.k, 0, 1, pool, shared, _p(yT),
+        assert L.moe_layer_forward(_p(x), T, _p(dl.router), moe.F32, None, cfg.k, 0, 1, pool, shared, None, _p(yT),
                                    None, None, None, None, _p(ws), need - 1, 0, s) == WS
         assert bool(torch.isnan(yT).all())
         assert int(ws.count_nonzero()) == 0
     # route: k larger than E
     ids = torch.full((2, cfg.k), -7, dtype=torch.int32, device="cuda")
     assert L.moe_route(_p(dl.x), None, 2, cfg.H, _p(dl.router), moe.F32, cfg.E, None, cfg.E + 1, 0, 1, _p(ids),
-                       _p(dl.w), None, _p(dl.ws_route), dl.ws_route.numel(), s) == INVALID
+                       _p(dl.w), None, None, None, _p(dl.ws_route), dl.ws_route.numel(), s) == INVALID
     torch.cuda.synchronize()
     assert bool(torch.isnan(y).all())
     assert int((ids == -7).sum()) == ids.numel()

@@ -573,3 +573,60 @@ def test_zipf_router_bias_skews_selection():
     u_plain = len(np.unique(oracle.topk(plain, small.k)[0]))
     u_skewed = len(np.unique(oracle.topk(skewed, small.k)[0]))
     assert u_skewed < u_plain, (u_skewed, u_plain)
+
+
+# ------------------------------------------------------- shared-expert gate
+# READING (oracle.c, oracle_expert_ffn): the shared expert's output is scaled
+# per token by sigma(w . x), w the f32 gate vector; without it the weight is 1.
+
+GATED = synth.shrink(synth.CONFIGS["a3b"], H=512, I=256, E=8, k=3, shared_I=256, shared_gate=True)
+
+
+def _parts(L):
+    """y with the shared expert left out, and with it at weight 1"""
+    xq = oracle.quantize(L.x)
+    logits = oracle.router_logits(L.router, L.x)
+    ids, w = oracle.topk(logits, L.cfg.k)
+    routed = oracle.expert_ffn(L, xq, ids, w, shared=False)["y"]
+    full = oracle.expert_ffn(L, xq, ids, w, shared=True)["y"]
+    return routed, full
+
+
+def test_shared_gate_zero_vector_halves_the_shared_expert():
+    L = synth.make_layer(GATED, 0, T=3)
+    L.shexp_gate = np.zeros(GATED.H, np.float32)           # sigma(0) = 1/2 exactly
+    routed, full = _parts(L)
+    res = oracle.layer_forward(L)
+    assert np.all(res["shared_scale"] == 0.5)
+    want = routed + 0.5 * (full - routed)
+    assert np.max(np.abs(res["y"] - want)) <= 1e-12 * np.abs(want).max()
+
+
+def test_shared_gate_saturates_to_one_and_zero():
+    L = synth.make_layer(GATED, 0, T=2)
+    routed, full = _parts(L)
+    # a gate along token 0's own hidden state, scaled up: logit +huge for it
+    L.shexp_gate = (1e4 * L.x[0]).astype(np.float32)
+    res = oracle.layer_forward(L)
+    assert res["shared_logit"][0] > 1e3 and res["shared_scale"][0] == 1.0
+    assert np.array_equal(res["y"][0], full[0])
+    L.shexp_gate = (-1e4 * L.x[0]).astype(np.float32)
+    res = oracle.layer_forward(L)
+    assert res["shared_scale"][0] < 1e-300
+    assert np.max(np.abs(res["y"][0] - routed[0])) <= 1e-12 * np.abs(routed[0]).max()
+
+
+def test_shared_gate_logit_against_fp64_dot_and_per_token_scale():
+    L = synth.make_layer(GATED, 1, T=4)
+    assert L.shexp_gate is not None and L.shexp_gate.shape == (GATED.H,)
+    res = oracle.layer_forward(L)
+    w64 = L.shexp_gate.astype(np.float64)
+    for t in range(4):
+        exact = float(np.dot(w64, L.x[t].astype(np.float64)))
+        bound = GATED.H * 2.0 ** -24 * float(np.dot(np.abs(w64), np.abs(L.x[t].astype(np.float64)))) * 2
+        assert abs(float(res["shared_logit"][t]) - exact) <= bound
+        assert res["shared_scale"][t] == 1.0 / (1.0 + np.exp(-float(res["shared_logit"][t])))
+    # y = routed + s_t * (full - routed) token by token
+    routed, full = _parts(L)
+    want = routed + res["shared_scale"][:, None] * (full - routed)
+    assert np.max(np.abs(res["y"] - want)) <= 1e-12 * np.abs(want).max()

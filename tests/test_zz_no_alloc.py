@@ -57,7 +57,7 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     pool = moe._Pool(moe.Q4_K, H, I, E, table.data_ptr())
     # T=16, k=32, I=4096: the h scratch alone is 8 MiB > 2 MiB
     rc = L.moe_expert_ffn_noalloc(xq.data_ptr(), T, ids.data_ptr(), w.data_ptr(), k, ctypes.byref(pool), None,
-                                  y.data_ptr(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+                                  None, y.data_ptr(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == 3, moe.status_str(rc)
     torch.cuda.synchronize()
     assert bool(torch.isnan(y).all())
