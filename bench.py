@@ -49,6 +49,10 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-overlap", action="store_true", help="launch layers without the overlap flag")
+    p.add_argument("--split", choices=["tokens", "experts"], default="tokens",
+                   help="tokens: every rank decodes its own tokens (replicas); experts: every rank holds the "
+                        "experts e with e %% world == rank (rank 0 also the shared expert) of the same layers, "
+                        "and each layer's partial outputs are gathered and summed in rank order")
     return p.parse_args()
 
 
@@ -72,6 +76,20 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def expert_owner_mask(E: int, rank: int, world: int) -> np.ndarray:
+    """Experts rank `rank` holds under the expert-parallel split: e % world == rank."""
+    return np.arange(E) % world == rank
+
+
+def rank_order_sum(parts):
+    """Host-side statement of the reduction moe_sum_partials performs on the
+    device: the partials added in rank order."""
+    y = np.array(parts[0], copy=True)
+    for p in parts[1:]:
+        y = y + p
+    return y
 
 
 def job_throughput(world: int, steps: int, layers: int, tokens: int, seconds: float) -> float:
@@ -258,7 +276,7 @@ class Stack:
     CUDA graphs: one fused launch per layer ("step"), the three calls per
     layer ("three") and the FFN call alone ("ffn")."""
 
-    def __init__(self, cfg, L, T, seed, dev, stream, overlap, keep_host=0):
+    def __init__(self, cfg, L, T, seed, dev, stream, overlap, keep_host=0, owned=None, with_shared=True):
         import torch
         import synth
         import quantized_routed_expert_router_gb300 as moe
@@ -268,7 +286,7 @@ class Stack:
         self.layers, self.host_sample = [], []
         for l in range(L):
             Lh = synth.make_layer(cfg, l, T=T, seed=seed)
-            self.layers.append(DeviceLayer(Lh, dev))
+            self.layers.append(DeviceLayer(Lh, dev, owned=owned, with_shared=with_shared))
             if l < keep_host:
                 self.host_sample.append(Lh)
             del Lh
@@ -351,6 +369,66 @@ def side_figures(S, K, W, stream, world, dev, peak):
         "hbm_gbs": gbs, "hbm_frac_of_measured": gbs / peak, "setup_s": S.gen_s}
 
 
+def run_expert_parallel(args, cfg, L, T, rank, world, local, dev, stream, peak, peak_src):
+    """Expert parallelism over the ranks: the same L layers and tokens on every
+    rank; rank r holds the experts with e % world == r (rank 0 also the shared
+    expert), runs the layer call on that pool (NULL entries: "not mine") and
+    gets a partial y; the partials of each layer are gathered and summed in
+    rank order (moe_sum_partials) before the next layer, as decode needs.
+    Eager launches (the gather is a collective between them)."""
+    import torch
+    import torch.distributed as dist
+    import quantized_routed_expert_router_gb300 as moe
+    owned = expert_owner_mask(cfg.E, rank, world)
+    S = Stack(cfg, L, T, args.seed, dev, stream, not args.no_overlap, owned=owned, with_shared=(rank == 0))
+    gathered = torch.empty((world, T, cfg.H), dtype=torch.float32, device=dev)
+    Yfull = torch.empty((L, T, cfg.H), dtype=torch.float32, device=dev)
+    flags = 0 if args.no_overlap else moe.LAYER_OVERLAP_PREVIOUS
+
+    def step():
+        for l, dl in enumerate(S.layers):
+            dl.forward_fused(flags=flags, outputs=False)
+            if world > 1:
+                dist.all_gather_into_tensor(gathered, dl.y)
+                moe.moe_sum_partials(gathered, Yfull[l])
+            else:
+                Yfull[l].copy_(dl.y)
+
+    K, W = args.steps, max(3, args.warmup)
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as cs:
+            e0.record(stream)
+            for _ in range(K):
+                step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    status = S.status()
+    if any(status):
+        raise RuntimeError(f"device status after the timed region: {status}")
+    if rank == 0:
+        value = K * L * T / (ms / 1e3)   # every rank served the same tokens
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+                "ms_per_step": ms / K, "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
+                "dtype": "int8", "data": "synthetic",
+                "config": {"workload": workload_name(cfg, L, T), "tokens": T, "layers": L,
+                           "parallelism": f"ep{world}: expert e on rank e % {world}, shared expert on rank 0, "
+                                          "partial y gathered and summed in rank order per layer",
+                           "us_per_layer": 1e3 * ms / (K * L), "setup_s": S.gen_s},
+                "cpu_baseline": None, "e2e": None, "gpu_launches": K * L * (2 if world > 1 else 1),
+                "clocks": cs.summary()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     import synth
@@ -372,6 +450,9 @@ def main():
     T = args.tokens
     stream = torch.cuda.Stream(device=dev)
     peak, peak_src = peaks()
+
+    if args.split == "experts":
+        return run_expert_parallel(args, cfg, L, T, rank, world, local, dev, stream, peak, peak_src)
 
     # ---- workload: L distinct layers, each rank its own tokens (seed offset)
     keep = 2 if (world == 1 and not args.no_cpu) else 0

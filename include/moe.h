@@ -74,6 +74,7 @@ typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID = 1 } moe_gating;
 #define MOE_MAX_TOKENS 16          /* T per call (small-batch decode)        */
 #define MOE_MAX_K 32               /* top-k                                  */
 #define MOE_MAX_EXPERTS 1024       /* E                                      */
+#define MOE_MAX_RANKS 64           /* partial outputs summed by moe_sum_partials */
 
 /* ------------------------------------------------------------------ sizes */
 
@@ -336,6 +337,21 @@ moe_status moe_layer_forward(const float *hidden, int T, const void *w_router, m
 size_t moe_layer_workspace_bytes(int T, int k, const moe_pool *pool, const moe_pool *shared);
 
 /*
+ * Expert-parallel reduction (README "MoE resolve": each tier card computes
+ * the slots of the experts it holds and the partial outputs are summed).  An
+ * expert-parallel rank passes moe_expert_ffn / moe_layer_forward a pool whose
+ * non-owned entries are NULL and gets a partial y; with the R partials side
+ * by side (for example gathered from every rank):
+ *   parts : device fp32 [R][n], rank r's partial at parts + r*n
+ *   y     : device fp32 [n] out: y[i] = ((parts[0][i] + parts[1][i]) + ...)
+ *           + parts[R-1][i], added in rank order, so the result does not
+ *           depend on how the partials arrived
+ * Both 16-byte aligned; n % 4 == 0; 1 <= R <= MOE_MAX_RANKS.
+ * Errors: MOE_ERR_INVALID_ARG for R, n or a NULL or unaligned buffer.
+ */
+moe_status moe_sum_partials(const float *parts, int R, size_t n, float *y, cudaStream_t stream);
+
+/*
  * Reads (and, if clear != 0, zeroes) the device status word at the start of
  * an FFN or layer workspace (both keep it in their first 4 bytes).
  * Synchronises `stream`.  *flags receives MOE_DEV_* bits.
@@ -353,6 +369,18 @@ moe_status moe_read_device_status(void *ws, int clear, uint32_t *flags, cudaStre
  */
 moe_status moe_debug_row_dots(const void *packed, moe_qtype qtype, int rows, int cols, int row,
                               const void *xq, int32_t *isums, cudaStream_t stream);
+
+/*
+ * Test hook: the bound, in SM clock cycles, on how long a moe_layer_forward
+ * launch made after this call waits for another block's exchange words
+ * (logits, h, o) before it gives up with MOE_DEV_TIMEOUT; 0 restores the
+ * default (8e8 cycles).  A short bound makes the timeout path run without
+ * any fault: the launch skips the remaining work, lets its own bulk copies
+ * land (those waits keep the long bound) and returns.  Host-side setting of
+ * this process, read when a layer launch is made (a captured graph keeps the
+ * value it was captured with).  Errors: MOE_ERR_INVALID_ARG for cycles < 0.
+ */
+moe_status moe_debug_set_exchange_wait(long long cycles);
 
 const char *moe_status_str(moe_status s);
 

@@ -23,7 +23,7 @@ MAX_TOKENS, MAX_K, MAX_EXPERTS = 16, 32, 1024
 EXPORTS = ["moe_act_block", "moe_q8_row_bytes", "moe_packed_bytes", "moe_pack_weights", "moe_quantize_q8K",
            "moe_route", "moe_route_workspace_bytes", "moe_expert_ffn", "moe_ffn_workspace_bytes",
            "moe_read_device_status", "moe_debug_row_dots", "moe_status_str", "moe_expert_ffn_noalloc",
-           "moe_layer_forward", "moe_layer_workspace_bytes"]
+           "moe_layer_forward", "moe_layer_workspace_bytes", "moe_sum_partials", "moe_debug_set_exchange_wait"]
 LAYER_OVERLAP_PREVIOUS = 0x1
 DEV_TIMEOUT = 0x4
 
@@ -89,6 +89,10 @@ def lib():
         L.moe_read_device_status.argtypes = [_P, i, ctypes.POINTER(ctypes.c_uint32), _P]
         L.moe_debug_row_dots.restype = i
         L.moe_debug_row_dots.argtypes = [_P, i, i, i, i, _P, _P, _P]
+        L.moe_sum_partials.restype = i
+        L.moe_sum_partials.argtypes = [_P, i, sz, _P, _P]
+        L.moe_debug_set_exchange_wait.restype = i
+        L.moe_debug_set_exchange_wait.argtypes = [ctypes.c_longlong]
         L.moe_status_str.restype = ctypes.c_char_p
         L.moe_status_str.argtypes = [i]
         _lib_handle = L
@@ -227,6 +231,20 @@ def moe_layer_forward(hidden, w_router, rtype: int, router_bias, k: int, gating:
                                    _ptr(y),
                                    _ptr(ids_out), _ptr(weights_out), _ptr(logits_out), _ptr(xq_out), _ptr(ws),
                                    ws.numel() * ws.element_size(), flags, _stream(stream)), "moe_layer_forward")
+
+
+def moe_sum_partials(parts, y, stream=None):
+    """y = the partial outputs parts [R, ...] summed in rank order (expert parallelism)."""
+    R = parts.shape[0]
+    n = y.numel()
+    if parts.numel() != R * n:
+        raise ValueError("parts must hold R partials of y's size")
+    _check(lib().moe_sum_partials(_ptr(parts), R, n, _ptr(y), _stream(stream)), "moe_sum_partials")
+
+
+def moe_debug_set_exchange_wait(cycles: int):
+    """Test hook: bound on a layer launch's waits for other blocks' words (0: default)."""
+    _check(lib().moe_debug_set_exchange_wait(int(cycles)), "moe_debug_set_exchange_wait")
 
 
 def moe_read_device_status(ws, clear: bool = True, stream=None) -> int:

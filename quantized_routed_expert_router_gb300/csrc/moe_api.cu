@@ -190,6 +190,13 @@ moe_status moe_expert_ffn(const void *xq, int T, const int32_t *ids, const float
     return cuda_status(launch_ffn(a, stream));
 }
 
+moe_status moe_sum_partials(const float *parts, int R, size_t n, float *y, cudaStream_t stream) {
+    if (R < 1 || R > MOE_MAX_RANKS || n % 4) return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    if (!parts || !y || !aligned16(parts) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_sum_partials(parts, R, n, y, stream));
+}
+
 moe_status moe_read_device_status(void *ws, int clear, uint32_t *flags, cudaStream_t stream) {
     if (!ws || !flags) return MOE_ERR_INVALID_ARG;
     uint32_t v = 0;

@@ -62,7 +62,10 @@ constexpr int MAX_LW = 16;
 constexpr int NBAR = 32;               // ring items in flight (barrier slots)
 constexpr int MAX_ITEM_RECS = 16;      // records per ring item, at most (also the empty-barrier count)
 // bound on every device-side wait, in SM clock cycles (about 0.4-1 s at the
-// clocks this part runs at); the cycle counter is cheap to poll
+// clocks this part runs at); the cycle counter is cheap to poll.  Waits for
+// another block's exchange words use the launch's wait_limit instead (this
+// value unless a test sets a shorter one); waits for this block's own bulk
+// copies always use this bound, so no block leaves with a copy in flight.
 constexpr long long WAIT_CYCLES = 800ll * 1000ll * 1000ll;
 
 // ------------------------------------------------------------ PTX helpers
@@ -192,12 +195,13 @@ static __device__ __noinline__ void fail_dev(Misc *m, unsigned *status) {
     atomicOr(status, MOE_DEV_TIMEOUT);
 }
 // p re-read until it carries epoch ep (bounded; on timeout the value is not used)
-static __device__ __noinline__ tword wait_tag_slow(const tword *p, uint32_t ep, Misc *m, unsigned *status) {
+static __device__ __noinline__ tword wait_tag_slow(const tword *p, uint32_t ep, Misc *m, unsigned *status,
+                                                   long long limit) {
     const long long t0 = clock64();
     for (;;) {
         const tword w = ld_tag(p);
         if (tag_of(w) == ep) return w;
-        if (m->abort || clock64() - t0 > WAIT_CYCLES) {
+        if (m->abort || clock64() - t0 > limit) {
             fail_dev(m, status);
             return w;
         }
@@ -350,7 +354,7 @@ struct LayerKernel {
 
     // w, already loaded from p, if it carries this launch's epoch, else p re-read
     __device__ __forceinline__ tword wait_tag(const tword *p, tword w) {
-        return tag_of(w) == ep ? w : wait_tag_slow(p, ep, m, a.status);
+        return tag_of(w) == ep ? w : wait_tag_slow(p, ep, m, a.status, a.wait_limit);
     }
 
     // ------------------------------------------------------------ units
@@ -624,7 +628,7 @@ struct LayerKernel {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) all &= tag_of(w[i]) == ep;
                 if (all) break;
-                if (m->abort || clock64() - t0 > WAIT_CYCLES) {
+                if (m->abort || clock64() - t0 > a.wait_limit) {
                     fail();
                     break;
                 }
@@ -910,7 +914,7 @@ struct LayerKernel {
 #pragma unroll
                         for (int jj = 0; jj < 8; ++jj)
                             if (jj < n) all &= tag_of(w[jj]) == ep;
-                        if (!all && (m->abort || clock64() - t0 > WAIT_CYCLES)) {
+                        if (!all && (m->abort || clock64() - t0 > a.wait_limit)) {
                             fail();
                             break;
                         }
@@ -1123,7 +1127,7 @@ struct LayerKernel {
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
                         if (q < cnt) all &= tag_of(w[q]) == ep;
-                    if (!all && (m->abort || clock64() - t0 > WAIT_CYCLES)) {
+                    if (!all && (m->abort || clock64() - t0 > a.wait_limit)) {
                         fail();
                         break;
                     }

@@ -82,8 +82,12 @@ static int lg_recs_per_item(size_t ring, uint32_t rec_bytes) {
     return r >= 8 ? 3 : (r >= 4 ? 2 : (r >= 2 ? 1 : 0));
 }
 
+static long long g_exchange_wait = 0;   // 0: the kernel's default bound
+void set_exchange_wait(long long cycles) { g_exchange_wait = cycles; }
+
 cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStream_t s) {
     if (!plan_fits(a, qtype, sqtype)) return cudaErrorNotSupported;
+    a.wait_limit = g_exchange_wait > 0 ? g_exchange_wait : 800ll * 1000ll * 1000ll;
     int G = num_sms();
     if (G > 256) G = 256;
     const int nseg = (a.H + 1023) / 1024;
@@ -212,6 +216,12 @@ SplitWs split_ws_layout(int T, int k, const moe_pool *pool, const moe_pool *shar
 }
 
 extern "C" {
+
+moe_status moe_debug_set_exchange_wait(long long cycles) {
+    if (cycles < 0) return MOE_ERR_INVALID_ARG;
+    set_exchange_wait(cycles);
+    return MOE_OK;
+}
 
 size_t moe_layer_workspace_bytes(int T, int k, const moe_pool *pool, const moe_pool *shared) {
     if (T < 1 || k < 1 || !pool) return 0;

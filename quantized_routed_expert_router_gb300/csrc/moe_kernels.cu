@@ -259,6 +259,36 @@ cudaError_t launch_shared_gate(const float *hidden, int T, int H, const float *w
     return cudaGetLastError();
 }
 
+// ------------------------------------------------- expert-parallel partials
+// y[i] = sum over ranks r = 0, 1, ... of parts[r][i], added in rank order
+// (README "MoE resolve": tier cards compute their slots and the partial
+// outputs are summed; a fixed order keeps the sum reproducible).
+__global__ void __launch_bounds__(256) sum_partials_kernel(const float4 *__restrict__ parts, int R, size_t n4,
+                                                           float4 *__restrict__ y) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        float4 s = parts[i];
+        for (int r = 1; r < R; ++r) {
+            const float4 v = parts[(size_t)r * n4 + i];
+            s.x = __fadd_rn(s.x, v.x);
+            s.y = __fadd_rn(s.y, v.y);
+            s.z = __fadd_rn(s.z, v.z);
+            s.w = __fadd_rn(s.w, v.w);
+        }
+        y[i] = s;
+    }
+}
+
+cudaError_t launch_sum_partials(const float *parts, int R, size_t n, float *y, cudaStream_t s) {
+    const size_t n4 = n / 4;
+    if (n4 == 0) return cudaSuccess;
+    size_t blocks = (n4 + 255) / 256;
+    const size_t cap = (size_t)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    sum_partials_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const float4 *>(parts), R, n4,
+                                                         reinterpret_cast<float4 *>(y));
+    return cudaGetLastError();
+}
+
 // ----------------------------------------------------------------- packing
 // One thread per (row, record): copies that row's bytes of the record from
 // the GGUF block row into the record's planes (layout stated in moe.h).

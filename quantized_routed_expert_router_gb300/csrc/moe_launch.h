@@ -74,6 +74,7 @@ struct LayerArgs {
     int bslots;                     // B-record partial-sum slots of the reduction buffer
     uint32_t ring_bytes;
     int lgra, lgrb;                 // log2 of the records per ring item: A (gate + up runs), B (down run)
+    long long wait_limit;           // cycles a wait for another block's exchange words may take
     size_t xrec, hrec;
     Smem sm;
 };
@@ -84,6 +85,8 @@ struct LayerWs {
 LayerWs layer_ws_layout(int T, int k, int H, int I, int Is, int E);
 // plans shared memory and launches the fused layer kernel for the pool's formats
 cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStream_t s);
+// the exchange-wait bound of later layer launches (0: the default)
+void set_exchange_wait(long long cycles);
 
 // every argument check of moe_expert_ffn except the workspace's (MOE_OK for
 // T == 0 once the shapes are valid)
@@ -103,6 +106,7 @@ cudaError_t launch_quantize(const float *x, int T, int n, uint8_t *xq, cudaStrea
 cudaError_t launch_route(const RouteArgs &a, int rtype, cudaStream_t s);
 // per-token weight of the shared expert (shared_gate_weight) into scale[T]
 cudaError_t launch_shared_gate(const float *hidden, int T, int H, const float *w, float *scale, cudaStream_t s);
+cudaError_t launch_sum_partials(const float *parts, int R, size_t n, float *y, cudaStream_t s);
 cudaError_t launch_pack(const uint8_t *src, int qtype, int rows, int cols, uint8_t *dst, cudaStream_t s);
 cudaError_t launch_row_dots(const uint8_t *packed, int qtype, int cols, int row, const uint8_t *xq,
                             int32_t *out, cudaStream_t s);

@@ -281,3 +281,17 @@ def test_route_shared_gate_weight(T, H):
                   shared_gate=to_dev(g), shared_scale=sc)
     torch.cuda.synchronize()
     assert np.allclose(sc.cpu().numpy(), want, rtol=1e-6, atol=0)
+
+
+def test_sum_partials_adds_in_rank_order():
+    """moe_sum_partials: y = ((p0 + p1) + p2) + ..., bit for bit the rank-order
+    fp32 sum, for an odd length of float4 groups and one rank."""
+    for R, n in ((3, 4 * 1001), (1, 64), (8, 4096 * 4)):
+        parts = synth.normal(5, R * 7 + n, 1.0, R, n)
+        want = parts[0].copy()
+        for r in range(1, R):
+            want = (want + parts[r]).astype(np.float32)
+        y = torch.full((n,), float("nan"), device=DEV)
+        moe.moe_sum_partials(to_dev(parts), y)
+        torch.cuda.synchronize()
+        assert np.array_equal(y.cpu().numpy(), want)

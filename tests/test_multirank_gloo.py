@@ -4,9 +4,12 @@ Two things are covered:
 
 - the benchmark's data-parallel rank logic: the rank environment, distinct
   token seeds per rank, max-over-ranks timing and the job-wide throughput;
-- the expert-ownership split of one layer. Rank r owns the experts with
-  e % 2 == r and rank 0 owns the shared expert; the partial y's are gathered
-  and summed in rank order, and the sum must equal the unsplit layer.
+- the expert-ownership split of one layer, through the benchmark's
+  expert-parallel host logic (``bench.expert_owner_mask``,
+  ``bench.rank_order_sum``): rank r owns the experts with e % 2 == r and
+  rank 0 owns the shared expert; the partial y's are gathered and summed in
+  rank order, and the sum must equal the unsplit layer - also with a gated
+  shared expert, whose weight applies on rank 0 only.
 
 The split follows the pulsar README's "MoE resolve" passage: a NULL expert
 pointer means "not mine", and the per-card partial results are summed. Here
@@ -48,19 +51,23 @@ def _worker(rank, world, port, out):
         xs = [torch.zeros(mine.x.shape, dtype=torch.float32) for _ in range(w)]
         dist.all_gather(xs, torch.from_numpy(np.ascontiguousarray(mine.x, dtype=np.float32)))
 
-        layer = synth.make_layer(cfg, 0, T=2, seed=0)   # the same layer on every rank
-        full = oracle.layer_forward(layer)
-        owned = np.arange(cfg.E) % w == rank
-        part = oracle.expert_ffn(layer, full["xq"], full["ids"], full["w"], owned=owned,
-                                 shared=(rank == 0))["y"]
-        parts = [torch.zeros(part.shape, dtype=torch.float64) for _ in range(w)]
-        dist.all_gather(parts, torch.from_numpy(np.ascontiguousarray(part, dtype=np.float64)))
-        y = parts[0].numpy().copy()
-        for i in range(1, w):   # fixed reduction order: rank order
-            y += parts[i].numpy()
-        err = float(np.max(np.abs(y - full["y"])))
+        errs = []
+        owned = bench.expert_owner_mask(cfg.E, rank, w)
+        for gated in (False, True):
+            c = synth.shrink(cfg, shared_gate=gated)
+            layer = synth.make_layer(c, 0, T=2, seed=0)   # the same layer on every rank
+            full = oracle.layer_forward(layer)
+            part = oracle.expert_ffn(layer, full["xq"], full["ids"], full["w"], owned=owned, shared=(rank == 0),
+                                     shared_scale=full["shared_scale"])["y"]
+            parts = [torch.zeros(part.shape, dtype=torch.float64) for _ in range(w)]
+            dist.all_gather(parts, torch.from_numpy(np.ascontiguousarray(part, dtype=np.float64)))
+            y = bench.rank_order_sum([p.numpy() for p in parts])
+            errs.append(float(np.max(np.abs(y - full["y"]))) / float(np.max(np.abs(full["y"]))))
+        masks = [torch.zeros(cfg.E, dtype=torch.uint8) for _ in range(w)]
+        dist.all_gather(masks, torch.from_numpy(owned.astype(np.uint8)))
+        cover = sum(m.numpy().astype(int) for m in masks)   # every expert on exactly one rank
         out.put((rank, r, w, local, slowest, rate,
-                 bool(np.array_equal(xs[0].numpy(), xs[1].numpy())), err, float(np.max(np.abs(full["y"])))))
+                 bool(np.array_equal(xs[0].numpy(), xs[1].numpy())), max(errs), bool(np.all(cover == 1))))
     finally:
         dist.destroy_process_group()
 
@@ -80,9 +87,10 @@ def test_two_gloo_ranks_rank_logic_and_expert_split():
         for p in procs:
             p.join(timeout=60)
     assert all(p.exitcode == 0 for p in procs)
-    for rank, (r, r_env, w, local, slowest, rate, same_x, err, ymax) in enumerate(res):
+    for rank, (r, r_env, w, local, slowest, rate, same_x, rel_err, cover) in enumerate(res):
         assert (r, r_env, w, local) == (rank, rank, 2, rank)
         assert slowest == 2.5                         # the slower rank's time on both ranks
         assert rate == 2 * 10 * 4 * 2 / 0.5           # every rank's layer-tokens count
         assert not same_x                             # each rank decodes its own tokens
-        assert err <= 1e-12 * ymax                    # the split sums to the unsplit layer
+        assert rel_err <= 1e-12                       # the split sums to the unsplit layer
+        assert cover                                  # the ownership masks partition the experts
