@@ -164,8 +164,17 @@ __device__ __forceinline__ void cbar_n() { asm volatile("bar.sync 1, %0;" ::"n"(
 
 // ------------------------------------------------------------- block state
 
+// The work plan's counts and this block's B range for U owned experts.
+struct SpecPlan {
+    int tilesI, tilesIs, tilesH, n_ra, nA, n_sb, n_rb, nB, brev, closed, jb0, jb1, nb;
+    uint32_t target, lo, hi;
+};
+
 struct Misc {
     volatile int abort;
+    volatile int spec_ready;   // one token: the producer's plan for U = k is in spec
+    int use_spec;
+    SpecPlan spec;
     int U, n_sa, n_ra, nA, n_sb, n_rb, nB, jb0, jb1;
     int tilesI, tilesIs, tilesH;
     uint32_t ep;         // this launch's epoch
@@ -178,7 +187,7 @@ struct Misc {
     // item and first record (relative to the batch; entry [n] holds the
     // totals) and hq slot
     int bt_j[64], bt_it[65], bt_rec[65], bt_slot[64];
-    uint32_t bsum[MAX_LW], target, lo, hi;   // B shares, in 128-byte lines
+    uint32_t bsum[MAX_LW], target, lo, hi;   // B shares, in quarters of 128-byte lines
     int closed;          // the B shares need no clamping (closed form)
     float sgate[4];      // per-token weight of the shared expert (with a gate vector)
     int brev;            // B ranges are given to blocks G-1 first
@@ -947,6 +956,7 @@ struct LayerKernel {
             }
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             m->abort = 0;
+            m->spec_ready = 0;
         }
         for (int i = threadIdx.x; i < NBAR; i += LT) tags()[i] = 0xFFFFFFFFu;
         __syncthreads();
@@ -1293,7 +1303,18 @@ struct LayerKernel {
                 }
         }
         cbar();
-        plan();
+        // one token, every chosen expert owned: the producer made this plan
+        // while the routing ran
+        if (threadIdx.x == 0) {
+            const bool use = NT == 1 && m->U == a.k && m->spec_ready;
+            if (use) {
+                __threadfence_block();   // the flag before the plan it publishes
+                put_plan(m->spec);
+            }
+            m->use_spec = use ? 1 : 0;
+        }
+        cbar();
+        if (!m->use_spec) plan();
         load_plan();
     }
 
@@ -1308,41 +1329,13 @@ struct LayerKernel {
     // finish lets them start at once.  So the B order over blocks runs
     // backwards when the last pass is a forward one.
     __device__ void plan() {
-        // bytes in 128-byte lines (every packed tile is a whole number of
-        // them), so all of it is 32-bit integer arithmetic: the host refuses
-        // shapes whose layer could reach 2^31 lines
         const uint32_t sa = 2u * (uint32_t)(FS::tile_bytes(a.H) >> 7), ra = 2u * (uint32_t)(F::tile_bytes(a.H) >> 7);
         const uint32_t sb = a.shared ? (uint32_t)(FS::tile_bytes(a.Is) >> 7) : 0u, rb = (uint32_t)(F::tile_bytes(a.I) >> 7);
         const int tid = threadIdx.x;
         if (tid == 0) {
-            m->tilesI = a.I / 32;
-            m->tilesIs = a.shared ? a.Is / 32 : 0;
-            m->tilesH = a.H / 32;
-            m->n_ra = m->U * m->tilesI;
-            m->nA = m->n_sa + m->n_ra;
-            m->n_sb = a.shared ? m->tilesH : 0;
-            m->n_rb = m->U * m->tilesH;
-            m->nB = m->n_sb + m->n_rb;
-            const uint32_t tot = (uint32_t)m->n_sa * sa + (uint32_t)m->n_ra * ra + (uint32_t)m->n_sb * sb +
-                                 (uint32_t)m->n_rb * rb;
-            const uint32_t target = tot / (uint32_t)G + 1u;   // any fixed rule works: all blocks agree
-            m->target = target;
-            // no block's A bytes exceed the mean: the shares need no clamping,
-            // and block c's share starts at c * target - (A bytes of blocks < c)
-            const int npass = (m->nA + G - 1) / G;
-            const uint32_t amax = (uint32_t)npass * (sa > ra ? sa : ra);
-            m->brev = npass > 0 && ((npass - 1) & 1) == 0;
-            m->closed = amax <= target;
-            if (m->closed) {
-                if (m->brev) {   // B order G-1, ..., 0: the blocks above c come first
-                    const uint32_t atot = a_before(G, sa, ra);
-                    m->lo = (uint32_t)(G - 1 - c) * target - (atot - a_before(c + 1, sa, ra));
-                    m->hi = (uint32_t)(G - c) * target - (atot - a_before(c, sa, ra));
-                } else {
-                    m->lo = (uint32_t)c * target - a_before(c, sa, ra);
-                    m->hi = (uint32_t)(c + 1) * target - a_before(c + 1, sa, ra);
-                }
-            }
+            SpecPlan s;
+            closed_plan(m->U, s);
+            put_plan(s);
         }
         cbar();
         if (!m->closed) {   // a block-wide scan of the clamped shares
@@ -1351,8 +1344,8 @@ struct LayerKernel {
             if (tid < G) {
                 for (int pass = 0; pass * G < m->nA; ++pass) {
                     const int j = snake_unit(pass, bc, G);
-                    if (j < m->n_sa) my_a += sa;
-                    else if (j < m->nA) my_a += ra;
+                    if (j < m->n_sa) my_a += (uint32_t)a.balpha * sa;
+                    else if (j < m->nA) my_a += (uint32_t)a.balpha * ra;
                 }
             }
             const uint32_t b = (tid < G && m->target > my_a) ? m->target - my_a : 0u;
@@ -1372,21 +1365,96 @@ struct LayerKernel {
             if (tid == pos + 1) m->hi = excl;
             cbar();
         }
-        if (tid == 0) {
+        if (tid == 0 && !m->closed) {   // the range from the scanned shares
             const bool last = m->brev ? c == 0 : c + 1 == G;   // last in B order
-            m->jb0 = first_b_unit(m->lo, sb, rb);
-            m->jb1 = last ? m->nB : first_b_unit(m->hi, sb, rb);
+            m->jb0 = first_b_unit(m->lo >> 2, sb, rb, m->n_sb, m->nB);
+            m->jb1 = last ? m->nB : first_b_unit(m->hi >> 2, sb, rb, m->n_sb, m->nB);
             if (m->jb1 < m->jb0) m->jb1 = m->jb0;
             m->nb = m->jb1 - m->jb0;
         }
         cbar();
     }
 
+    // The plan for U owned experts, by one thread: unit counts, the B order,
+    // and - when no block's weighted A bytes exceed the mean share, so no
+    // share needs clamping (s.closed) - this block's B range in closed form.
+    // Bytes in 128-byte lines (every packed tile is a whole number of them),
+    // shares in quarter lines: 32-bit integers throughout (the host refuses
+    // shapes whose layer could reach 2^28 lines).
+    __device__ void closed_plan(int U, SpecPlan &s) {
+        const uint32_t sa = 2u * (uint32_t)(FS::tile_bytes(a.H) >> 7), ra = 2u * (uint32_t)(F::tile_bytes(a.H) >> 7);
+        const uint32_t sb = a.shared ? (uint32_t)(FS::tile_bytes(a.Is) >> 7) : 0u, rb = (uint32_t)(F::tile_bytes(a.I) >> 7);
+        const int n_sa = a.shared ? a.Is / 32 : 0;
+        s.tilesI = a.I / 32;
+        s.tilesIs = a.shared ? a.Is / 32 : 0;
+        s.tilesH = a.H / 32;
+        s.n_ra = U * s.tilesI;
+        s.nA = n_sa + s.n_ra;
+        s.n_sb = a.shared ? s.tilesH : 0;
+        s.n_rb = U * s.tilesH;
+        s.nB = s.n_sb + s.n_rb;
+        // A bytes count a.balpha quarters in the balance: a block's B
+        // records wait in its ring until its own A work is done, so its B
+        // work lands mostly after its A work however the bytes are split
+        const uint32_t aq = (uint32_t)a.balpha;
+        const uint32_t tot = aq * ((uint32_t)n_sa * sa + (uint32_t)s.n_ra * ra) +
+                             4u * ((uint32_t)s.n_sb * sb + (uint32_t)s.n_rb * rb);
+        const uint32_t target = tot / (uint32_t)G + 1u;   // any fixed rule works: all blocks agree
+        s.target = target;
+        // block c's share starts at c * target - (weighted A bytes of blocks < c)
+        const int npass = (s.nA + G - 1) / G;
+        const uint32_t amax = aq * (uint32_t)npass * (sa > ra ? sa : ra);
+        s.brev = npass > 0 && ((npass - 1) & 1) == 0;
+        s.closed = amax <= target;
+        s.lo = s.hi = 0u;
+        s.jb0 = s.jb1 = s.nb = 0;
+        if (!s.closed) return;
+        if (s.brev) {   // B order G-1, ..., 0: the blocks above c come first
+            const uint32_t atot = aq * a_before(G, sa, ra, n_sa, s.nA);
+            s.lo = (uint32_t)(G - 1 - c) * target - (atot - aq * a_before(c + 1, sa, ra, n_sa, s.nA));
+            s.hi = (uint32_t)(G - c) * target - (atot - aq * a_before(c, sa, ra, n_sa, s.nA));
+        } else {
+            s.lo = (uint32_t)c * target - aq * a_before(c, sa, ra, n_sa, s.nA);
+            s.hi = (uint32_t)(c + 1) * target - aq * a_before(c + 1, sa, ra, n_sa, s.nA);
+        }
+        const bool last = s.brev ? c == 0 : c + 1 == G;   // last in B order
+        s.jb0 = first_b_unit(s.lo >> 2, sb, rb, s.n_sb, s.nB);
+        s.jb1 = last ? s.nB : first_b_unit(s.hi >> 2, sb, rb, s.n_sb, s.nB);
+        if (s.jb1 < s.jb0) s.jb1 = s.jb0;
+        s.nb = s.jb1 - s.jb0;
+    }
+    __device__ void put_plan(const SpecPlan &s) {
+        m->tilesI = s.tilesI;
+        m->tilesIs = s.tilesIs;
+        m->tilesH = s.tilesH;
+        m->n_ra = s.n_ra;
+        m->nA = s.nA;
+        m->n_sb = s.n_sb;
+        m->n_rb = s.n_rb;
+        m->nB = s.nB;
+        m->brev = s.brev;
+        m->closed = s.closed;
+        m->target = s.target;
+        m->lo = s.lo;
+        m->hi = s.hi;
+        m->jb0 = s.jb0;
+        m->jb1 = s.jb1;
+        m->nb = s.nb;
+    }
+
     // A lines of blocks [0, c) under the snake deal: pass p gives them units
     // [pG, pG + c) (even p) or [pG + G - c, pG + G) (odd p); units below
     // n_sa are shared-expert units of sa lines, the rest up to nA routed of ra
-    __device__ uint32_t a_before(int cc, uint32_t sa, uint32_t ra) {
-        const int n_sa = m->n_sa, nA = m->nA;
+    __device__ uint32_t a_before(int cc, uint32_t sa, uint32_t ra, int n_sa, int nA) {
+        if (n_sa < G) {
+            // closed form: every full pass gives each block one unit; the last,
+            // partial pass (rem units) goes to blocks 0.. (forward) or ..G-1
+            // (backward); the shared units are the first n_sa of pass 0
+            const int P = nA / G, rem = nA - P * G;
+            const int part = (P & 1) == 0 ? min(cc, rem) : max(0, cc - (G - rem));
+            const int units = cc * P + part, sh = min(cc, n_sa);
+            return sa * (uint32_t)sh + ra * (uint32_t)(units - sh);
+        }
         auto span = [](int lo, int hi, int a0, int a1) -> uint32_t {
             const int l = lo > a0 ? lo : a0, h = hi < a1 ? hi : a1;
             return h > l ? (uint32_t)(h - l) : 0u;
@@ -1406,8 +1474,7 @@ struct LayerKernel {
 
     // first B unit whose midpoint is >= X (B list: shared units of sb lines,
     // then routed units of rb lines; midpoints in half lines)
-    __device__ int first_b_unit(uint32_t X, uint32_t sb, uint32_t rb) {
-        const int n_sb = m->n_sb, nB = m->nB;
+    __device__ int first_b_unit(uint32_t X, uint32_t sb, uint32_t rb, int n_sb, int nB) {
         const uint32_t X2 = 2u * X;
         auto mid2 = [&](int j) -> uint32_t {
             return j < n_sb ? (2u * (uint32_t)j + 1u) * sb : 2u * (uint32_t)n_sb * sb + (2u * (uint32_t)(j - n_sb) + 1u) * rb;
@@ -1457,26 +1524,21 @@ struct LayerKernel {
                 if (tb) bulk_g2s(sm + o.table, a.experts, tb, fixed_bar());
             }
         }
-        // This block's shared-expert units come first in its snake passes.
-        // Their items go out now as far as the empty ring holds them: the
-        // consumers take them only after the routing, so nothing is reclaimed
-        // before the handoff, and a request that had to wait for room would
-        // never be served.  (spass, sq): the first item not yet requested.
-        int spass = 0, sq = 0;
+        // this block's shared-expert units (its first snake passes): the
+        // consumers run them while the routing completes, freeing the ring
         if (lane == 0) {
-            for (; spass * G < p.n_sa && !m->abort; ++spass, sq = 0) {
-                const int j = snake_unit(spass, c, G);
-                if (j >= p.n_sa) break;   // later passes hold routed units only
-                Unit U;
-                unit_of(j, U);
-                for (; sq < U.nitems; ++sq) {
-                    int r0, r1;
-                    item_recs(U, sq, r0, r1);
-                    const uint32_t run = run_bytes(U, r0, r1);
-                    if (R.issued >= NBAR || R.head + 2 * run > a.ring_bytes) break;
-                    issue(R, U, sq);
-                }
-                if (sq < U.nitems) break;
+            for (int pass = 0; pass * G < p.n_sa && !m->abort; ++pass) {
+                const int j = snake_unit(pass, c, G);
+                if (j < p.n_sa && !issue_unit(R, j)) break;
+            }
+        }
+        if (NT == 1 && lane == 0 && !m->abort) {   // the plan for U = k, off the routing path
+            SpecPlan s;
+            closed_plan(a.k, s);
+            if (s.closed) {
+                m->spec = s;
+                __threadfence_block();
+                m->spec_ready = 1;
             }
         }
         if (lane == 0 && a.shared) m->shx = *a.shared;   // for units after the handoff
@@ -1484,11 +1546,9 @@ struct LayerKernel {
         shp = &m->shx;
         load_plan();
         if (lane == 0 && !m->abort) {
-            // the remaining shared-expert items, then the routed units
-            for (int pass = spass; pass * G < p.nA; ++pass) {
+            for (int pass = 0; pass * G < p.nA; ++pass) {   // the routed units
                 const int j = snake_unit(pass, c, G);
-                if (j >= p.nA) continue;
-                if (!issue_unit(R, j, pass == spass ? sq : 0)) break;
+                if (j >= p.n_sa && j < p.nA && !issue_unit(R, j)) break;
             }
             for (int n = 0; n < p.nb && !m->abort; ++n)
                 if (!issue_unit(R, b_unit(n))) break;
@@ -1514,7 +1574,26 @@ struct LayerKernel {
         cbar();
         ep = m->ep;
         router_logits();
-        route_tail(xq_first);
+        // the shared expert's gate/up units while the other blocks publish
+        // their logits (x quantised first)
+        bool x_done = xq_first;
+        int item = 0, ua = 0;
+        if (p.n_sa > 0) {
+            if (!x_done) {
+                quantise_x(0);
+                cbar();
+                x_done = true;
+            }
+            for (int pass = 0; pass * G < p.n_sa; ++pass) {
+                const int j = snake_unit(pass, c, G);
+                if (j < p.n_sa) {
+                    Unit U;
+                    unit_of(j, U);
+                    run_A<FS>(U, item, ua);
+                }
+            }
+        }
+        route_tail(x_done);
         if (c == 0 && a.xq_out) {
             const int n16 = (int)(a.xrec / 16);
             for (int i = threadIdx.x; i < a.T * n16; i += LW * 32)
@@ -1522,16 +1601,12 @@ struct LayerKernel {
         }
         bar_handoff();
         gating_weights();
-        // A units in ring order: this block's shared-expert units (their
-        // records were requested before the routing), then its routed ones
-        int item = 0, ua = 0;
-        for (int pass = 0; pass * G < p.nA; ++pass) {
+        for (int pass = 0; pass * G < p.nA; ++pass) {   // the routed A units
             const int j = snake_unit(pass, c, G);
-            if (j < p.nA) {
+            if (j >= p.n_sa && j < p.nA) {
                 Unit U;
                 unit_of(j, U);
-                if (std::is_same<F, FS>::value || j >= p.n_sa) run_A<F>(U, item, ua);
-                else run_A<FS>(U, item, ua);
+                run_A<F>(U, item, ua);
             }
         }
         // no loop below leaves early: every consumer thread must reach every

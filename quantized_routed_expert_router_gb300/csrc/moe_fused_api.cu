@@ -62,12 +62,12 @@ static size_t tile_bytes_of(int q, int cols) {
 }
 
 // The kernel's work plan counts bytes in 128-byte lines with 32-bit
-// integers: every expert of the call at once must stay below 2^30 lines.
+// integers: every expert of the call at once must stay below 2^28 lines.
 static bool plan_fits(const LayerArgs &a, int qtype, int sqtype) {
     const size_t P = (size_t)a.T * a.k;
     size_t lines = P * (2 * tile_bytes_of(qtype, a.H) * (size_t)(a.I / 32) + tile_bytes_of(qtype, a.I) * (size_t)(a.H / 32));
     if (a.shared) lines += 2 * tile_bytes_of(sqtype, a.H) * (size_t)(a.Is / 32) + tile_bytes_of(sqtype, a.Is) * (size_t)(a.H / 32);
-    return (lines >> 7) < ((size_t)1 << 30);
+    return (lines >> 7) < ((size_t)1 << 28);   // x4 (quarter lines) stays below 2^30
 }
 
 // smallest possible ring item of a format: a gate+up record pair, or one down record
@@ -88,6 +88,7 @@ void set_exchange_wait(long long cycles) { g_exchange_wait = cycles; }
 cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStream_t s) {
     if (!plan_fits(a, qtype, sqtype)) return cudaErrorNotSupported;
     a.wait_limit = g_exchange_wait > 0 ? g_exchange_wait : 800ll * 1000ll * 1000ll;
+    a.balpha = 2;   // A bytes count half (measured on the 235B-A22B-style layer: 0.5 beats 0 and 1)
     int G = num_sms();
     if (G > 256) G = 256;
     const int nseg = (a.H + 1023) / 1024;

@@ -75,6 +75,7 @@ struct LayerArgs {
     uint32_t ring_bytes;
     int lgra, lgrb;                 // log2 of the records per ring item: A (gate + up runs), B (down run)
     long long wait_limit;           // cycles a wait for another block's exchange words may take
+    int balpha;                     // weight of A bytes in the B-range balance, in quarters (0..4)
     size_t xrec, hrec;
     Smem sm;
 };
