@@ -651,22 +651,46 @@ struct LayerKernel {
     __device__ int load_hq_batch(int n0, int nend) {
         int *kbase = m->kslot;
         int *keys = m->kkey;
-        if (threadIdx.x == 0) {
-            int nk = 0, used = 0, n = n0;
-            for (; n < nend && n - n0 < 64; ++n) {
-                const int key = b_key(b_unit(n));
-                bool seen = false;
-                for (int q = 0; q < nk; ++q) seen |= keys[q] == key;
-                if (seen) continue;
-                const int need = key_pairs(key);
-                if ((used + need > a.hq_slots || nk == 64) && n > n0) break;
-                keys[nk] = key;
-                kbase[nk] = used;
-                used += need;
-                ++nk;
+        if (warp == 0) {
+            // units from n0 in order: a unit whose expert differs from the
+            // previous unit's brings that expert (B ranges are contiguous, so
+            // each expert's units are consecutive); the batch ends before the
+            // first new expert whose pairs would overflow the hq slots or
+            // that would be the 65th, and after 64 units.  Lane l takes unit
+            // base + l; prefix sums over the lanes stand in for a serial walk.
+            int nk = 0, used = 0, n = n0, prev_key = -1;
+            for (int base = n0; base < nend && base - n0 < 64; base += 32) {
+                const int i = base + lane;
+                const bool valid = i < nend && i - n0 < 64;
+                const int key = valid ? b_key(b_unit(i)) : -2;
+                const int up = __shfl_up_sync(0xFFFFFFFFu, key, 1);
+                const bool isnew = valid && key != (lane == 0 ? prev_key : up);
+                const int need = isnew ? key_pairs(key) : 0;
+                int cn = need, ck = isnew ? 1 : 0;   // inclusive prefix sums
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int vn = __shfl_up_sync(0xFFFFFFFFu, cn, off), vk = __shfl_up_sync(0xFFFFFFFFu, ck, off);
+                    if (lane >= off) { cn += vn; ck += vk; }
+                }
+                const bool brk = isnew && i > n0 && (used + cn > a.hq_slots || nk + ck > 64);
+                const unsigned stop = __ballot_sync(0xFFFFFFFFu, brk || !valid);
+                const int first = stop ? __ffs(stop) - 1 : 32;   // units base .. base + first - 1 join
+                if (lane < first && isnew) {
+                    keys[nk + ck - 1] = key;
+                    kbase[nk + ck - 1] = used + cn - need;
+                }
+                if (first > 0) {
+                    used += __shfl_sync(0xFFFFFFFFu, cn, first - 1);
+                    nk += __shfl_sync(0xFFFFFFFFu, ck, first - 1);
+                    prev_key = __shfl_sync(0xFFFFFFFFu, key, first - 1);
+                }
+                n = base + first;
+                if (first < 32) break;
             }
-            m->nkeys = nk;
-            m->bend = n;
+            if (lane == 0) {
+                m->nkeys = nk;
+                m->bend = n;
+            }
         }
         cbar();
         if (warp == 0) b_table(n0, m->bend);   // the batch's unit table, while h is still arriving
