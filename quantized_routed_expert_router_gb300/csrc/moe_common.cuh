@@ -103,6 +103,26 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
     return __dp4a((int)a, (int)b, c);
 }
+// c + sum over the four byte lanes of a (unsigned) times b (signed): lets a
+// code field be masked in place (the dot of 2^s x code) instead of shifted
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// c + a.lo16 * b.byte0 + a.hi16 * b.byte1 (lo), or times b.byte2, b.byte3 (hi);
+// a's halves signed, b's bytes unsigned.  Two int16 block sums of the
+// activation record times two unsigned scale bytes in one instruction.
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 
 __device__ __forceinline__ int4 lds128(const int8_t *p) { return *reinterpret_cast<const int4 *>(p); }
 
@@ -161,11 +181,14 @@ struct FQ4K {
             is[2 * g] = dp4a(q.y & 0x0F0F0F0Fu, (uint32_t)xl.y, is[2 * g]);
             is[2 * g] = dp4a(q.z & 0x0F0F0F0Fu, (uint32_t)xl.z, is[2 * g]);
             is[2 * g] = dp4a(q.w & 0x0F0F0F0Fu, (uint32_t)xl.w, is[2 * g]);
-            is[2 * g + 1] = dp4a((q.x >> 4) & 0x0F0F0F0Fu, (uint32_t)xh.x, is[2 * g + 1]);
-            is[2 * g + 1] = dp4a((q.y >> 4) & 0x0F0F0F0Fu, (uint32_t)xh.y, is[2 * g + 1]);
-            is[2 * g + 1] = dp4a((q.z >> 4) & 0x0F0F0F0Fu, (uint32_t)xh.z, is[2 * g + 1]);
-            is[2 * g + 1] = dp4a((q.w >> 4) & 0x0F0F0F0Fu, (uint32_t)xh.w, is[2 * g + 1]);
+            // high nibbles masked in place: the bytes are 16 x code
+            is[2 * g + 1] = dp4a_us(q.x & 0xF0F0F0F0u, (uint32_t)xh.x, is[2 * g + 1]);
+            is[2 * g + 1] = dp4a_us(q.y & 0xF0F0F0F0u, (uint32_t)xh.y, is[2 * g + 1]);
+            is[2 * g + 1] = dp4a_us(q.z & 0xF0F0F0F0u, (uint32_t)xh.z, is[2 * g + 1]);
+            is[2 * g + 1] = dp4a_us(q.w & 0xF0F0F0F0u, (uint32_t)xh.w, is[2 * g + 1]);
         }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) is[2 * g + 1] >>= 4;   // exact: a multiple of 16
     }
     // d_x * (d * sum_j sc_j is_j - dmin * sum_j m_j bsum32_j)
     __device__ static float combine(const W &w, const Act &a, int k0, int, const int *is) {
@@ -174,13 +197,23 @@ struct FQ4K {
         const uint32_t sc47 = (s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u);
         const uint32_t m47 = ((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u);
         int P = 0, M = 0;
-        const int16_t *bs = a.bs + (k0 >> 4);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            P += (int)byte_of(sc03, j) * is[j] + (int)byte_of(sc47, j) * is[4 + j];
-            M += (int)byte_of(m03, j) * ((int)bs[2 * j] + (int)bs[2 * j + 1]) +
-                 (int)byte_of(m47, j) * ((int)bs[8 + 2 * j] + (int)bs[8 + 2 * j + 1]);
-        }
+        for (int j = 0; j < 4; ++j) P += (int)byte_of(sc03, j) * is[j] + (int)byte_of(sc47, j) * is[4 + j];
+        // sum_j m_j * (the two 16-element block sums of sub-block j): word j
+        // of the block-sum array holds that pair as int16, so one dp2a takes
+        // a sub-block against its min byte, replicated into the byte pair
+        const int8_t *bs = reinterpret_cast<const int8_t *>(a.bs + (k0 >> 4));
+        const int4 b03 = lds128(bs), b47 = lds128(bs + 16);
+        const uint32_t m01 = prmt(m03, 0, 0x1100u), m23 = prmt(m03, 0, 0x3322u);
+        const uint32_t m45 = prmt(m47, 0, 0x1100u), m67 = prmt(m47, 0, 0x3322u);
+        M = dp2a_lo((uint32_t)b03.x, m01, M);
+        M = dp2a_hi((uint32_t)b03.y, m01, M);
+        M = dp2a_lo((uint32_t)b03.z, m23, M);
+        M = dp2a_hi((uint32_t)b03.w, m23, M);
+        M = dp2a_lo((uint32_t)b47.x, m45, M);
+        M = dp2a_hi((uint32_t)b47.y, m45, M);
+        M = dp2a_lo((uint32_t)b47.z, m67, M);
+        M = dp2a_hi((uint32_t)b47.w, m67, M);
         const float d = h2f(w.c[0].x), dmin = h2f(w.c[0].x >> 16);
         const float dx = a.d[k0 >> a.lgB];
         return dx * (d * (float)P - dmin * (float)M);
@@ -221,24 +254,33 @@ struct FQ2K {
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const int4 xv = lds128(x + 128 * n + 32 * s + 16 * h);
+                // field s masked in place: the bytes are 4^s x code
+                const uint32_t mk = 0x03030303u << (2 * s);
                 int acc = 0;
-                acc = dp4a((q.x >> (2 * s)) & 0x03030303u, (uint32_t)xv.x, acc);
-                acc = dp4a((q.y >> (2 * s)) & 0x03030303u, (uint32_t)xv.y, acc);
-                acc = dp4a((q.z >> (2 * s)) & 0x03030303u, (uint32_t)xv.z, acc);
-                acc = dp4a((q.w >> (2 * s)) & 0x03030303u, (uint32_t)xv.w, acc);
-                is[8 * n + 2 * s + h] = acc;
+                acc = dp4a_us(q.x & mk, (uint32_t)xv.x, acc);
+                acc = dp4a_us(q.y & mk, (uint32_t)xv.y, acc);
+                acc = dp4a_us(q.z & mk, (uint32_t)xv.z, acc);
+                acc = dp4a_us(q.w & mk, (uint32_t)xv.w, acc);
+                is[8 * n + 2 * s + h] = acc >> (2 * s);   // exact: a multiple of 4^s
             }
         }
     }
     __device__ static float combine(const W &w, const Act &a, int k0, int, const int *is) {
-        const int16_t *bs = a.bs + (k0 >> 4);
         const uint32_t sw[4] = {w.s.x, w.s.y, w.s.z, w.s.w};
+        // block sums of the 16 sub-blocks as 8 words of int16 pairs
+        const int8_t *bs = reinterpret_cast<const int8_t *>(a.bs + (k0 >> 4));
+        const int4 b0 = lds128(bs), b1 = lds128(bs + 16);
+        const uint32_t bw[8] = {(uint32_t)b0.x, (uint32_t)b0.y, (uint32_t)b0.z, (uint32_t)b0.w,
+                                (uint32_t)b1.x, (uint32_t)b1.y, (uint32_t)b1.z, (uint32_t)b1.w};
         int P = 0, M = 0;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const uint32_t b = byte_of(sw[j >> 2], j & 3);
-            P += (int)(b & 15u) * is[j];
-            M += (int)(b >> 4) * (int)bs[j];
+        for (int q = 0; q < 4; ++q) {
+            // scale byte j = 4q + t: low nibble scale, high nibble min
+            const uint32_t sc = sw[q] & 0x0F0F0F0Fu, mn = (sw[q] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) P += (int)prmt(sc, 0, 0x4440u + t) * is[4 * q + t];
+            M = dp2a_lo(bw[2 * q], mn, M);
+            M = dp2a_hi(bw[2 * q + 1], mn, M);
         }
         const float d = h2f(w.dd), dmin = h2f(w.dd >> 16);
         const float dx = a.d[k0 >> a.lgB];
@@ -356,9 +398,11 @@ struct FMX4 {
             const uint32_t x1 = __byte_perm(xaw[k], xbw[k], 0x7362);
             // positive codes: magnitude; negative codes: bit 3 set -> sign of a
             // table byte (all zero) -> 0.  Flipped codes give the converse.
-            pos = dp4a(prmt(LUT0, LUT1, wq & 0xFFFFu), x0, pos);
+            // prmt reads only the low four selector nibbles, so the low half
+            // of a code word needs no mask.
+            pos = dp4a(prmt(LUT0, LUT1, wq), x0, pos);
             pos = dp4a(prmt(LUT0, LUT1, wq >> 16), x1, pos);
-            neg = dp4a(prmt(LUT0, LUT1, wn & 0xFFFFu), x0, neg);
+            neg = dp4a(prmt(LUT0, LUT1, wn), x0, neg);
             neg = dp4a(prmt(LUT0, LUT1, wn >> 16), x1, neg);
         }
         return pos - neg;
