@@ -297,7 +297,7 @@ moe_status moe_expert_ffn_noalloc(const void *xq, int T, const int32_t *ids, con
  * selects the same top-k and streams its share of the chosen experts' packed
  * weights with TMA bulk copies into a shared-memory ring.  Logits, h and the
  * per-slot o rows pass between blocks through the workspace as 8-byte words
- * that carry the value and a per-call epoch (a launch counter kept in the
+ * that carry the value and a per-call epoch (launch counters kept in the
  * workspace), so readers poll the data itself.  Results equal those of the
  * three calls (same arithmetic and summation orders).
  *   hidden      : device fp32 [T][H]; w_router/rtype/router_bias/k/gating/

@@ -35,10 +35,11 @@
 //  polls the words it needs, re-reading all the missing ones each round,
 //  until they carry the epoch.  An 8-byte aligned
 //  access is single-copy atomic, so a word with the right epoch holds the
-//  right value and no fence is needed on either side.  The epoch is a counter
-//  in the workspace, read by every block after the dependency wait; the last
-//  block to read it (an arrival count beside it) writes it back (+1), so no
-//  block can see the next value early.
+//  right value and no fence is needed on either side.  The epoch comes
+//  from one counter per block in the workspace: block c reads its own after
+//  the dependency wait and writes it back (+1) as it ends.  Every block
+//  advances its counter once per launch, so all blocks agree on the epoch, and
+//  no block touches another's counter.
 //  Every wait is bounded (SM cycle counter); a timeout sets MOE_DEV_TIMEOUT,
 //  drains this block's copies in flight and returns.
 #pragma once
@@ -148,17 +149,9 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const unsigned *p) {
 __device__ __forceinline__ void st_relaxed_u32(unsigned *p, uint32_t v) {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-// This launch's epoch: the stored counter + 1.  Each block then counts its
-// read (acq_rel: the read is ordered before the count).  The count's result
-// is only looked at when the block ends (finish), so the round trip stays off
-// the routing path; the block that completed the count has seen every
-// block's read, and stores the new epoch and clears the count for the next
-// launch, which reads both only after this grid is done.
-__device__ __forceinline__ uint32_t count_epoch_read(unsigned *arrive) {
-    uint32_t n;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(n) : "l"(arrive) : "memory");
-    return n;
-}
+// A line of global memory into L2 (no value comes back, so it may run before
+// the dependency wait: the later loads still read L2, the point of coherence)
+__device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 template <int LW>
 __device__ __forceinline__ void cbar_n() { asm volatile("bar.sync 1, %0;" ::"n"(LW * 32) : "memory"); }   // consumers only
 
@@ -304,7 +297,6 @@ struct LayerKernel {
     Misc *m;
     int c, G, warp, lane;
     uint32_t ep = 0;   // consumers: this launch's epoch (after the dependency wait)
-    uint32_t arrived = 0;   // thread 0: blocks that had read the epoch before this one
     Plan p;            // loaded by load_plan once the plan is in shared memory
     // the shared expert's table entry: the caller's device table until the
     // routing handoff, then the block's shared-memory copy of it
@@ -1003,7 +995,9 @@ struct LayerKernel {
         }
     }
 
-    __device__ void router_logits() {
+    // ep0: the block's launch counter as loaded by thread 0 (in flight until
+    // the dots are done)
+    __device__ void router_logits(uint32_t ep0) {
         int e0, e1;
         router_range(e0, e1);
         const int nr = e1 - e0;
@@ -1083,7 +1077,9 @@ struct LayerKernel {
                 }
             }
         }
+        if (threadIdx.x == 0) m->ep = ep0 + 1u;
         cbar();
+        ep = m->ep;
         for (int it = threadIdx.x; it < nr * a.T; it += LW * 32) {
             const int r = it / a.T, t = it - r * a.T;
             float l = segv[(r * nseg) * a.T + t];
@@ -1585,19 +1581,24 @@ struct LayerKernel {
     }
 
     __device__ void consumer() {
+        // the block's launch counter and (one block) the hidden rows into L2
+        // while the previous kernel runs
+        if (threadIdx.x == 0) prefetch_l2(a.epoch + c);
+        if (c == 0)
+            for (int i = 32 * threadIdx.x; i < a.T * a.H; i += 32 * 32 * LW) prefetch_l2(a.x + i);
         pdl_wait();
-        if (threadIdx.x == 0) {
-            m->ep = ld_relaxed_u32(a.epoch) + 1u;
-            arrived = count_epoch_read(a.arrive);
-        }
+        // This launch's epoch: the block's own counter + 1.  Every block
+        // advances its counter once per launch (finish), so all blocks agree
+        // without a shared count; the next launch reads it only after this
+        // grid is done.  The load is consumed after the router dots.
+        uint32_t ep0 = 0;
+        if (threadIdx.x == 0) ep0 = ld_relaxed_u32(a.epoch + c);
         // an fp32 router needs only x: its logits go out first and x is
         // quantised while the other blocks publish theirs; a Q8_0 router dots
-        // the quantised x
+        // the quantised x (router_logits' barrier orders it before the dots)
         const bool xq_first = a.rtype == MOE_Q8_0;
         if (xq_first) quantise_x(0);
-        cbar();
-        ep = m->ep;
-        router_logits();
+        router_logits(ep0);
         // the shared expert's gate/up units while the other blocks publish
         // their logits (x quantised first)
         bool x_done = xq_first;
@@ -1646,10 +1647,7 @@ struct LayerKernel {
     }
 
     __device__ void finish() {
-        if (threadIdx.x == 0 && arrived + 1u == (uint32_t)G) {
-            st_relaxed_u32(a.arrive, 0u);
-            st_relaxed_u32(a.epoch, m->ep);
-        }
+        if (threadIdx.x == 0) st_relaxed_u32(a.epoch + c, m->ep);
     }
 };
 

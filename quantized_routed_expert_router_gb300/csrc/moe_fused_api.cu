@@ -25,9 +25,8 @@ LayerWs layer_ws_layout(int T, int k, int H, int I, int Is, int E) {
     const size_t P = (size_t)T * k;
     LayerWs w;
     w.status = 0;
-    w.epoch = 64;
-    w.arrive = 128;
-    w.logits = 256;
+    w.epoch = 256;                   // one launch counter per block (G <= 256)
+    w.logits = w.epoch + 4 * 256;
     w.h_r = al(w.logits + 8 * (size_t)T * E);
     w.h_s = al(w.h_r + 8 * P * I);
     w.o_r = al(w.h_s + 8 * (size_t)T * (Is > 0 ? Is : 0));
@@ -286,7 +285,6 @@ moe_status moe_layer_forward(const float *hidden, int T, const void *w_router, m
     a.xq_out = (uint8_t *)xq_out;
     a.status = (unsigned *)(w + L.status);
     a.epoch = (unsigned *)(w + L.epoch);
-    a.arrive = (unsigned *)(w + L.arrive);
     typedef unsigned long long tw;
     a.logits = (tw *)(w + L.logits);
     a.h_r = (tw *)(w + L.h_r);

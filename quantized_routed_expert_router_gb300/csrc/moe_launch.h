@@ -63,7 +63,7 @@ struct LayerArgs {
     float *w_out;
     float *logits_out;
     uint8_t *xq_out;
-    unsigned *status, *epoch, *arrive;   // workspace: status word, launch counter, epoch readers
+    unsigned *status, *epoch;   // workspace: status word, per-block launch counters [G]
     // tagged words (value bits | epoch << 32): logits [T][E], h [T*k][I],
     // shared h [T][Is], o [T*k][H], shared o [T][H]
     unsigned long long *logits, *h_r, *h_s, *o_r, *o_s;
@@ -81,7 +81,7 @@ struct LayerArgs {
 };
 
 struct LayerWs {
-    size_t status, epoch, arrive, logits, h_r, h_s, o_r, o_s, total;
+    size_t status, epoch, logits, h_r, h_s, o_r, o_s, total;
 };
 LayerWs layer_ws_layout(int T, int k, int H, int I, int Is, int E);
 // plans shared memory and launches the fused layer kernel for the pool's formats
