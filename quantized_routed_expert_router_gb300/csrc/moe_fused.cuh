@@ -366,9 +366,13 @@ struct LayerKernel {
         const moe_expert *ex;
     };
 
+    // log2 of the records per ring item of a unit kind (each format sizes its own)
+    __device__ __forceinline__ int lg_of(int kind) const {
+        return kind == 0 ? a.lgsa : (kind == 1 ? a.lgra : (kind == 2 ? a.lgsb : a.lgrb));
+    }
     __device__ void unit_of(int j, Unit &U) {
         unit_of0(j, U);
-        const int lg = U.kind <= 1 ? a.lgra : a.lgrb;
+        const int lg = lg_of(U.kind);
         U.nitems = (U.nrec + (1 << lg) - 1) >> lg;
     }
     __device__ void unit_of0(int j, Unit &U) {
@@ -406,11 +410,11 @@ struct LayerKernel {
         }
     }
 
-    // Ring item q of a unit: records [r0, r1) with r0 = q R (R = 2^a.lgra for
-    // A units, 2^a.lgrb for B units).  An A item holds the gate run, then the up run
-    // of the same records; a B item holds the down run.
+    // Ring item q of a unit: records [r0, r1) with r0 = q R (R = 2^lg_of(kind)).
+    // An A item holds the gate run, then the up run of the same records; a B
+    // item holds the down run.
     __device__ void item_recs(const Unit &U, int q, int &r0, int &r1) {
-        const int lg = U.kind <= 1 ? a.lgra : a.lgrb;
+        const int lg = lg_of(U.kind);
         r0 = q << lg;
         r1 = min(r0 + (1 << lg), U.nrec);
     }
@@ -533,10 +537,11 @@ struct LayerKernel {
             tok[i] = (i < U.nt) ? (U.kind == 0 ? i : plist()[uoff()[U.u] + i] / a.k) : 0;
         // Record r's gate and up records both go to warp r % LW, which frees
         // the ring slot once it has read them both (during the up dot).
+        const int lg = lg_of(U.kind);
         for (int r = warp; r < U.nrec; r += LW) {
             int r0, r1;
-            item_recs(U, r >> a.lgra, r0, r1);
-            const int it = item + (r >> a.lgra);
+            item_recs(U, r >> lg, r0, r1);
+            const int it = item + (r >> lg);
             const uint8_t *base = wait_item(it);
             if (!base) continue;
             const uint8_t *rec = base + run_off<FF>(a.H, r0, r);
@@ -785,7 +790,8 @@ struct LayerKernel {
     template <class FF>
     __device__ void run_B_record(const Unit &U, int it0, int slot0, int r, int t) {
         const int Irows = U.kind == 2 ? a.Is : a.I;
-        const int q = r >> a.lgrb, r0 = q << a.lgrb;
+        const int lg = lg_of(U.kind);
+        const int q = r >> lg, r0 = q << lg;
         float pt[NT];
         int sidx[NT];
 #pragma unroll
@@ -813,7 +819,8 @@ struct LayerKernel {
             if (q < n1) {
                 const int j = b_unit(q), key = b_key(j);
                 nr[h] = key == MAXP ? FS::nrec(a.Is) : F::nrec(a.I);
-                ni[h] = (nr[h] + (1 << a.lgrb) - 1) >> a.lgrb;
+                const int lg = key == MAXP ? a.lgsb : a.lgrb;
+                ni[h] = (nr[h] + (1 << lg) - 1) >> lg;
                 m->bt_j[k] = j;
                 m->bt_slot[k] = key_slot(key);
             }

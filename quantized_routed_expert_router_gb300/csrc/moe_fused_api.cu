@@ -140,16 +140,12 @@ cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStre
     if (ring < 2 * (size_t)item) ring = 2 * (size_t)item;
     if (fixed_rest + ring > optin) ring = (optin - fixed_rest) & ~(size_t)127;
     a.ring_bytes = (uint32_t)ring;
-    {
-        uint32_t pa = 2 * max_rec(qtype, a.H), pb = max_rec(qtype, a.I);
-        if (a.shared) {
-            const uint32_t sa = 2 * max_rec(sqtype, a.H), sb = max_rec(sqtype, a.Is);
-            if (sa > pa) pa = sa;
-            if (sb > pb) pb = sb;
-        }
-        a.lgra = lg_recs_per_item(ring, pa);
-        a.lgrb = lg_recs_per_item(ring, pb);
-    }
+    // items per format: a small routed record (Q2_K) beside a large shared one
+    // (Q8_0) still gets copies of several records
+    a.lgra = lg_recs_per_item(ring, 2 * max_rec(qtype, a.H));
+    a.lgrb = lg_recs_per_item(ring, max_rec(qtype, a.I));
+    a.lgsa = a.shared ? lg_recs_per_item(ring, 2 * max_rec(sqtype, a.H)) : 0;
+    a.lgsb = a.shared ? lg_recs_per_item(ring, max_rec(sqtype, a.Is)) : 0;
     o.ring = take(ring);
     o.bars = take((2 * kNBAR + 5) * 8);   // ring full/empty, fixed bytes, A partials ready/free x 2
     o.starts = take(2 * kNBAR * 4);   // item start offsets, then slot tags

@@ -73,7 +73,8 @@ struct LayerArgs {
     int hq_slots;                   // q8 records of requantised h the block can hold
     int bslots;                     // B-record partial-sum slots of the reduction buffer
     uint32_t ring_bytes;
-    int lgra, lgrb;                 // log2 of the records per ring item: A (gate + up runs), B (down run)
+    int lgra, lgrb, lgsa, lgsb;     // log2 of the records per ring item: routed A (gate + up runs),
+                                    // routed B (down run), shared A, shared B
     long long wait_limit;           // cycles a wait for another block's exchange words may take
     int balpha;                     // weight of A bytes in the B-range balance, in quarters (0..4)
     size_t xrec, hrec;
