@@ -87,7 +87,7 @@ void set_exchange_wait(long long cycles) { g_exchange_wait = cycles; }
 cudaError_t launch_layer(LayerArgs &a, int qtype, int sqtype, bool pdl, cudaStream_t s) {
     if (!plan_fits(a, qtype, sqtype)) return cudaErrorNotSupported;
     a.wait_limit = g_exchange_wait > 0 ? g_exchange_wait : 800ll * 1000ll * 1000ll;
-    a.balpha = 2;   // A bytes count half (measured on the 235B-A22B-style layer: 0.5 beats 0 and 1)
+    a.balpha = 3;   // A bytes count three quarters (235B-A22B-style layer: measured against 0, 1/4, 1/2 and 1)
     int G = num_sms();
     if (G > 256) G = 256;
     const int nseg = (a.H + 1023) / 1024;
